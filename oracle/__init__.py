@@ -1,0 +1,190 @@
+"""CPU oracle for MoE expert-parallel dispatch / combine (ctypes over moe_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product library (``combine_layout_gb300``) never imports it and shares no code
+with it.
+
+Each wrapper follows a passage of the source pages (cited in moe_oracle.c):
+  route    -- "NVSHMEM 与 DeepEP：GPU 发起的通信", section "高吞吐模式" (node-limited
+              routing: 4 nodes by the sum of each node's top-2 scores, then top-8)
+  layout   -- same page, "高吞吐模式" (count tokens per rank and expert) and
+              "低延迟模式" (fixed slots); "NCCL EP 论文解读", "算法模式"/"Tensor Layouts"
+  dispatch -- same pages: HT 2D / LL 3D expert-major receive layout, FP8 e4m3 with
+              one fp32 scale per 128 elements ("高吞吐模式")
+  combine  -- "NCCL EP 论文解读", "核心功能函数" (un-permute with the handle's routing
+              state and reduce to token order); "高吞吐模式" (BF16 weighted sum)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoeoracle.so")
+
+OK, ERR_INVALID, ERR_OVERFLOW = 0, 1, 2
+MODE_LL, MODE_HT = 0, 1
+W_SOFTMAX_TOPK, W_SOFTMAX_RENORM, W_SCORE_NORM = 0, 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into libmoeoracle.so (plain gcc, IEEE arithmetic)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "moe_oracle.h"))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    i64, i32 = ctypes.c_int64, ctypes.c_int
+    lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_bf16_to_double.restype = ctypes.c_double
+    lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
+    lib.orc_bf16_from_double.restype = ctypes.c_uint16
+    lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_to_double.restype = ctypes.c_double
+    lib.orc_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.orc_e4m3_from_float.restype = ctypes.c_uint8
+    lib.orc_e4m3_from_float_array.argtypes = [P, i64, P]
+    lib.orc_e4m3_from_float_array.restype = None
+    lib.orc_quant_row.argtypes = [P, i32, P, P]
+    lib.orc_route.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P]
+    lib.orc_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
+    lib.orc_dispatch.argtypes = [P, i64, i32, i32, P, i64, i32, P, P, P]
+    lib.orc_combine.argtypes = [P, i64, i32, P, P, i64, i32, P, i64, P]
+    for f in ("orc_quant_row", "orc_route", "orc_layout", "orc_dispatch", "orc_combine"):
+        getattr(lib, f).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- scalars
+def bf16_to_double(b: int) -> float:
+    return _load().orc_bf16_to_double(int(b))
+
+
+def bf16_from_double(v: float) -> int:
+    return int(_load().orc_bf16_from_double(float(v)))
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().orc_e4m3_to_double(int(code))
+
+
+def e4m3_from_float(v: float) -> int:
+    return int(_load().orc_e4m3_from_float(float(v)))
+
+
+def e4m3_from_float_array(v) -> np.ndarray:
+    v = _c(v, np.float32).reshape(-1)
+    out = np.empty(v.shape, np.uint8)
+    _load().orc_e4m3_from_float_array(_p(v), v.size, _p(out))
+    return out
+
+
+def quant_row(x_bf16_bits) -> tuple[np.ndarray, np.ndarray]:
+    x = _c(x_bf16_bits, np.uint16).reshape(-1)
+    H = x.size
+    q = np.empty(H, np.uint8)
+    s = np.empty(max(H // 128, 1), np.float32)
+    st = _load().orc_quant_row(_p(x), H, _p(q), _p(s))
+    if st != OK:
+        raise ValueError(f"orc_quant_row status {st}")
+    return q, s[: H // 128]
+
+
+# ---------------------------------------------------------------- path
+def route(scores, k: int, num_groups: int = 1, topk_groups: int = 1,
+          group_topk: int = 0, weight_mode: int = W_SCORE_NORM):
+    """Node-limited top-k routing. Returns (topk_idx int32 [T,k], topk_w float64 [T,k])."""
+    s = _c(scores, np.float32)
+    T, E = s.shape
+    if group_topk == 0:
+        group_topk = -(-k // topk_groups)
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    st = _load().orc_route(_p(s), T, E, num_groups, topk_groups, group_topk, k,
+                           weight_mode, _p(idx), _p(w))
+    if st != OK:
+        raise ValueError(f"orc_route status {st}")
+    return idx, w
+
+
+def layout(topk_idx, experts: int, ranks: int, mode: int, slots: int = 0):
+    """Counts, offsets and the row map. Returns (dict, status)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    cnt = np.empty(experts, np.int32)
+    off = np.empty(experts + 1, np.int32)
+    rcnt = np.empty(ranks, np.int32)
+    roff = np.empty(ranks + 1, np.int32)
+    row = np.empty((T, k), np.int32)
+    st = _load().orc_layout(_p(idx), T, k, experts, ranks, mode, slots,
+                            _p(cnt), _p(off), _p(rcnt), _p(roff), _p(row))
+    return dict(cnt=cnt, off=off, rcnt=rcnt, roff=roff, row=row), st
+
+
+def dispatch(x_bf16_bits, row, nrows: int, fp8: bool, recv_x=None, recv_scale=None,
+             recv_src=None):
+    """Pack tokens into the receive layout. Returns (recv_x, recv_scale, recv_src)."""
+    x = _c(x_bf16_bits, np.uint16)
+    T, H = x.shape
+    row = _c(row, np.int32)
+    k = row.shape[1]
+    if recv_x is None:
+        recv_x = np.zeros((nrows, H), np.uint8 if fp8 else np.uint16)
+    if recv_scale is None:
+        recv_scale = np.zeros((nrows, max(H // 128, 1)), np.float32)
+    if recv_src is None:
+        recv_src = np.full(nrows, -1, np.int32)
+    st = _load().orc_dispatch(_p(x), T, H, k, _p(row), nrows, int(bool(fp8)),
+                              _p(recv_x), _p(recv_scale), _p(recv_src))
+    if st != OK:
+        raise ValueError(f"orc_dispatch status {st}")
+    return recv_x, recv_scale, recv_src
+
+
+def combine(y_bf16_bits, row, w, tokens=None) -> np.ndarray:
+    """Weighted un-permute back to token order. Returns bf16 bits [T or len(tokens), H]."""
+    y = _c(y_bf16_bits, np.uint16)
+    nrows, H = y.shape
+    row = _c(row, np.int32)
+    T, k = row.shape
+    w = _c(w, np.float32)
+    if tokens is None:
+        tk, ntok, n = None, 0, T
+    else:
+        tk = _c(tokens, np.int64).reshape(-1)
+        ntok = n = tk.size
+    out = np.empty((n, H), np.uint16)
+    st = _load().orc_combine(_p(y), nrows, H, _p(row), _p(w), T, k,
+                             None if tk is None else _p(tk), ntok, _p(out))
+    if st != OK:
+        raise ValueError(f"orc_combine status {st}")
+    return out

@@ -1,0 +1,348 @@
+/*
+ * moe_oracle.c -- plain, slow, single-threaded CPU oracle for MoE expert-parallel
+ * routing, layout, dispatch (optionally FP8) and combine.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference leg, never by the product library.
+ * It shares no code with the CUDA path.  Build: gcc -O2 -ffp-contract=off
+ * (no fast-math), so every fp32 / binary64 operation below is one IEEE
+ * operation, rounded to nearest.
+ *
+ * Sources (see moe_oracle.h for the full list):
+ *  - "NVSHMEM 与 DeepEP：GPU 发起的通信", section "高吞吐模式": node-limited routing
+ *    (keep 4 nodes by the sum of each node's two best expert scores, then pick 8
+ *    experts among them), contiguous expert -> GPU -> node placement, FP8
+ *    dispatch with one fp32 scale per 128 elements, BF16 combine of the
+ *    weighted sum of expert outputs.
+ *  - same page, section "低延迟模式": fixed slots per (local expert, source).
+ *  - "NCCL EP 论文解读", items "算法模式" and "Tensor Layouts": HT 2D output
+ *    [total_recv_tokens x hidden] in deterministic order with per-expert counts,
+ *    LL 3D expert-major output; "核心功能函数": combine un-permutes with the
+ *    routing state of the handle and reduces back to token order.
+ *
+ * parity pins: every function here is pinned by tests under tests/ (page
+ * statistics, brute force, closed forms, hand-worked FP8 cases).
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* bf16                                                                       */
+/* ------------------------------------------------------------------------- */
+
+static float bits_to_float(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t float_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+double orc_bf16_to_double(uint16_t b) { return (double)bits_to_float((uint32_t)b << 16); }
+
+static float bf16_to_float(uint16_t b) { return bits_to_float((uint32_t)b << 16); }
+
+/* Round a binary64 value to the nearest bf16 (8 significant bits, exponent
+ * range of fp32, subnormal spacing 2^-133), ties to even, in one step. */
+uint16_t orc_bf16_from_double(double v)
+{
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 8;                /* spacing of bf16 values near a */
+    if (q < -133) q = -133;       /* subnormal range */
+    double n = ldexp(a, -q);      /* exact: a / 2^q */
+    double fl = floor(n);
+    double rem = n - fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double r = ldexp(fl, q);
+    if (r >= ldexp(1.0, 128)) return sign | 0x7F80;   /* overflow -> inf */
+    uint32_t u = float_to_bits((float)r);             /* exact */
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------- */
+/* e4m3fn                                                                     */
+/* ------------------------------------------------------------------------- */
+
+double orc_e4m3_to_double(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9)          /* m/8 * 2^-6 */
+                        : ldexp((double)(8 + m), e - 10); /* (1+m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+uint8_t orc_e4m3_from_float(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    if (isnan(v)) return sign | 0x7F;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;   /* saturate to the largest finite value */
+    /* Largest non-negative code whose value is <= a (codes 0..0x7E are
+     * ordered by value). */
+    int lo = 0, hi = 0x7E;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (orc_e4m3_to_double((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    double below = orc_e4m3_to_double((uint8_t)lo);
+    double above = orc_e4m3_to_double((uint8_t)(lo + 1));  /* lo + 1 <= 0x7E */
+    double dl = a - below, du = above - a;                 /* both exact */
+    int c;
+    if (dl < du) c = lo;
+    else if (du < dl) c = lo + 1;
+    else c = (lo & 1) ? lo + 1 : lo;                       /* tie: even code */
+    return sign | (uint8_t)c;
+}
+
+void orc_e4m3_from_float_array(const float* v, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_from_float(v[i]);
+}
+
+int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale)
+{
+    if (H <= 0 || H % 128 != 0) return ORC_ERR_INVALID;
+    for (int b = 0; b < H / 128; ++b) {
+        const uint16_t* xb = x + (int64_t)b * 128;
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float a = fabsf(bf16_to_float(xb[i]));
+            if (a > amax) amax = a;
+        }
+        float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;   /* fp32 division */
+        scale[b] = s;
+        for (int i = 0; i < 128; ++i) {
+            float r = bf16_to_float(xb[i]) / s;            /* fp32 division */
+            q[(int64_t)b * 128 + i] = orc_e4m3_from_float(r);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* routing                                                                    */
+/* ------------------------------------------------------------------------- */
+
+typedef struct { double v; int i; } scored;
+
+/* (value descending, index ascending) */
+static int by_value_desc(const void* pa, const void* pb)
+{
+    const scored* a = (const scored*)pa;
+    const scored* b = (const scored*)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->i > b->i) - (a->i < b->i);
+}
+
+/* (value ascending, index descending): the first entries are the ones to ban */
+static int by_value_asc_index_desc(const void* pa, const void* pb)
+{
+    const scored* a = (const scored*)pa;
+    const scored* b = (const scored*)pb;
+    if (a->v < b->v) return -1;
+    if (a->v > b->v) return 1;
+    return (a->i < b->i) - (a->i > b->i);
+}
+
+static int double_asc(const void* pa, const void* pb)
+{
+    double a = *(const double*)pa, b = *(const double*)pb;
+    return (a > b) - (a < b);
+}
+
+int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k,
+              int weight_mode, int32_t* topk_idx, double* topk_w)
+{
+    if (T < 0 || E <= 0 || G <= 0 || E % G != 0 || kg < 1 || kg > G || k < 1 || k > E)
+        return ORC_ERR_INVALID;
+    const int gs = E / G;
+    const int limit = (G > 1 && kg < G);
+    if ((int64_t)kg * gs < k) return ORC_ERR_INVALID;
+    if (limit && (m < 1 || m > gs)) return ORC_ERR_INVALID;
+    if (weight_mode < ORC_W_SOFTMAX_TOPK || weight_mode > ORC_W_SCORE_NORM) return ORC_ERR_INVALID;
+
+    char* allowed = (char*)malloc((size_t)E);
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)gs);
+    scored* nodes = (scored*)malloc(sizeof(scored) * (size_t)G);
+    scored* cand = (scored*)malloc(sizeof(scored) * (size_t)E);
+
+    for (int64_t t = 0; t < T; ++t) {
+        const float* s = scores + t * E;
+        for (int e = 0; e < E; ++e) allowed[e] = 1;
+
+        /* Step 1 (node limit): score every node by the sum of its m best
+         * expert scores, then ban the G - kg lowest-scoring nodes. */
+        if (limit) {
+            for (int n = 0; n < G; ++n) {
+                for (int i = 0; i < gs; ++i) tmp[i] = (double)s[n * gs + i];
+                qsort(tmp, (size_t)gs, sizeof(double), double_asc);
+                double sum = 0.0;
+                for (int i = gs - m; i < gs; ++i) sum += tmp[i];   /* ascending order */
+                nodes[n].v = sum;
+                nodes[n].i = n;
+            }
+            qsort(nodes, (size_t)G, sizeof(scored), by_value_asc_index_desc);
+            for (int b = 0; b < G - kg; ++b) {
+                int n = nodes[b].i;
+                for (int i = 0; i < gs; ++i) allowed[n * gs + i] = 0;
+            }
+        }
+
+        /* Step 2: the k best allowed experts, best first. */
+        int nc = 0;
+        for (int e = 0; e < E; ++e)
+            if (allowed[e]) { cand[nc].v = (double)s[e]; cand[nc].i = e; ++nc; }
+        qsort(cand, (size_t)nc, sizeof(scored), by_value_desc);
+        for (int j = 0; j < k; ++j) topk_idx[t * k + j] = cand[j].i;
+
+        /* Step 3: gate weights (binary64). */
+        double* w = topk_w + t * k;
+        if (weight_mode == ORC_W_SCORE_NORM) {
+            double den = 0.0;
+            for (int j = 0; j < k; ++j) den += cand[j].v;
+            for (int j = 0; j < k; ++j) w[j] = cand[j].v / den;
+        } else if (weight_mode == ORC_W_SOFTMAX_TOPK) {
+            double mx = cand[0].v, den = 0.0;
+            for (int j = 0; j < k; ++j) den += exp(cand[j].v - mx);
+            for (int j = 0; j < k; ++j) w[j] = exp(cand[j].v - mx) / den;
+        } else {
+            double mx = (double)s[0];
+            for (int e = 1; e < E; ++e) if ((double)s[e] > mx) mx = (double)s[e];
+            double z = 0.0;
+            for (int e = 0; e < E; ++e) z += exp((double)s[e] - mx);
+            double sel = 0.0;
+            for (int j = 0; j < k; ++j) { w[j] = exp(cand[j].v - mx) / z; sel += w[j]; }
+            for (int j = 0; j < k; ++j) w[j] = w[j] / sel;
+        }
+    }
+    free(allowed); free(tmp); free(nodes); free(cand);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* layout                                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* 1 = the pair gets a row, 0 = masked (-1), -1 = invalid input */
+static int pair_kind(const int32_t* idx_row, int j, int E)
+{
+    int32_t e = idx_row[j];
+    if (e == -1) return 0;
+    if (e < -1 || e >= E) return -1;
+    for (int jj = 0; jj < j; ++jj)
+        if (idx_row[jj] == e) return -1;   /* repeated expert within the token */
+    return 1;
+}
+
+int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
+               int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0) return ORC_ERR_INVALID;
+    if (mode != ORC_MODE_LL && mode != ORC_MODE_HT) return ORC_ERR_INVALID;
+    if (mode == ORC_MODE_LL && S < 1) return ORC_ERR_INVALID;
+    const int L = E / R;
+    int status = ORC_OK;
+
+    /* Pass 1: tokens bound for every expert. */
+    for (int e = 0; e < E; ++e) cnt[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int kind = pair_kind(topk_idx + t * k, j, E);
+            if (kind < 0) status = ORC_ERR_INVALID;
+            if (kind == 1) cnt[topk_idx[t * k + j]] += 1;
+        }
+    off[0] = 0;
+    for (int e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+    for (int r = 0; r < R; ++r) {
+        rcnt[r] = 0;
+        for (int l = 0; l < L; ++l) rcnt[r] += cnt[r * L + l];
+    }
+    roff[0] = 0;
+    for (int r = 0; r < R; ++r) roff[r + 1] = roff[r] + rcnt[r];
+
+    /* Pass 2: each pair's place, tokens of one expert in ascending order. */
+    int32_t* cursor = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int64_t p = t * k + j;
+            if (pair_kind(topk_idx + t * k, j, E) != 1) { row[p] = -1; continue; }
+            int e = topk_idx[p];
+            int rank = cursor[e]++;
+            if (mode == ORC_MODE_HT) {
+                row[p] = off[e] + rank;
+            } else if (rank < S) {
+                row[p] = e * S + rank;
+            } else {
+                row[p] = -1;
+                status = ORC_ERR_OVERFLOW;
+            }
+        }
+    free(cursor);
+    return status;
+}
+
+/* ------------------------------------------------------------------------- */
+/* dispatch                                                                   */
+/* ------------------------------------------------------------------------- */
+
+int orc_dispatch(const uint16_t* x, int64_t T, int H, int k, const int32_t* row, int64_t nrows,
+                 int fp8, void* recv_x, float* recv_scale, int32_t* recv_src)
+{
+    if (T < 0 || H <= 0 || k < 1) return ORC_ERR_INVALID;
+    if (fp8 && H % 128 != 0) return ORC_ERR_INVALID;
+    const int nb = H / 128;
+    uint8_t* q = fp8 ? (uint8_t*)malloc((size_t)H) : NULL;
+    float* sc = fp8 ? (float*)malloc(sizeof(float) * (size_t)(nb > 0 ? nb : 1)) : NULL;
+    int status = ORC_OK;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* xt = x + t * H;
+        if (fp8) orc_quant_row(xt, H, q, sc);
+        for (int j = 0; j < k; ++j) {
+            int64_t r = row[t * k + j];
+            if (r < 0) continue;
+            if (r >= nrows) { status = ORC_ERR_INVALID; continue; }
+            if (fp8) {
+                memcpy((uint8_t*)recv_x + r * H, q, (size_t)H);
+                memcpy(recv_scale + r * nb, sc, sizeof(float) * (size_t)nb);
+            } else {
+                memcpy((uint16_t*)recv_x + r * H, xt, sizeof(uint16_t) * (size_t)H);
+            }
+            recv_src[r] = (int32_t)t;
+        }
+    }
+    free(q); free(sc);
+    return status;
+}
+
+/* ------------------------------------------------------------------------- */
+/* combine                                                                    */
+/* ------------------------------------------------------------------------- */
+
+int orc_combine(const uint16_t* y, int64_t nrows, int H, const int32_t* row, const float* w,
+                int64_t T, int k, const int64_t* tokens, int64_t ntok, uint16_t* out)
+{
+    if (T < 0 || H <= 0 || k < 1) return ORC_ERR_INVALID;
+    int64_t n = tokens ? ntok : T;
+    int status = ORC_OK;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) { status = ORC_ERR_INVALID; continue; }
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t r = row[t * k + j];
+                if (r < 0) continue;
+                if (r >= nrows) { status = ORC_ERR_INVALID; continue; }
+                acc += (double)w[t * k + j] * orc_bf16_to_double(y[r * H + h]);
+            }
+            out[i * H + h] = orc_bf16_from_double(acc);
+        }
+    }
+    return status;
+}

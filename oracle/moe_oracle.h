@@ -1,0 +1,92 @@
+/*
+ * moe_oracle.h -- plain, slow, single-threaded CPU oracle for MoE expert-parallel
+ * dispatch / combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the CPU
+ * baseline / reference leg of the benchmark may load this library.  The product
+ * (libmoeep) shares no code, header, table or constant with it.
+ *
+ * Every function follows a passage of the source pages:
+ *   "NVSHMEM 与 DeepEP：GPU 发起的通信" (anrans.github.io ai-infra-handbooks,
+ *       section "高吞吐模式" for node-limited routing, the expert -> GPU -> node
+ *       placement and FP8 with one fp32 scale per 128 elements; section
+ *       "低延迟模式" for the fixed LL slots),
+ *   "NCCL EP 论文解读" (lpnh.cn, items "核心功能函数", "算法模式", "Tensor Layouts"
+ *       for the HT 2D / LL 3D expert-major layouts and the combine that
+ *       un-permutes and reduces back to token order).
+ * Readings of points the pages leave open are stated next to each function.
+ *
+ * Status codes returned by the functions below.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_OK = 0, ORC_ERR_INVALID = 1, ORC_ERR_OVERFLOW = 2 };
+enum { ORC_MODE_LL = 0, ORC_MODE_HT = 1 };
+enum { ORC_W_SOFTMAX_TOPK = 0, ORC_W_SOFTMAX_RENORM = 1, ORC_W_SCORE_NORM = 2 };
+
+/* bf16 <-> binary64. bf16 -> double is exact; double -> bf16 rounds once,
+ * to nearest, ties to even. */
+double   orc_bf16_to_double(uint16_t b);
+uint16_t orc_bf16_from_double(double v);
+
+/* OCP e4m3fn (bias 7, largest finite 448, no infinity, NaN = S.1111.111). */
+double   orc_e4m3_to_double(uint8_t code);
+/* Round to nearest, ties to even; finite magnitudes beyond 448 (and infinities)
+ * saturate to +-448; NaN -> 0x7F with the sign kept. */
+uint8_t  orc_e4m3_from_float(float v);
+void     orc_e4m3_from_float_array(const float* v, int64_t n, uint8_t* out);
+
+/* Quantise one token row of H bf16 values (H % 128 == 0): per block of 128,
+ * amax = max |x|, scale = amax / 448 (fp32 division; 1 when amax == 0),
+ * q = e4m3(x / scale) with fp32 division. */
+int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale);
+
+/* Node-limited (grouped) top-k routing, then gate weights in binary64.
+ * scores [T][E] fp32; E experts in G contiguous groups (nodes) of E/G.
+ * If 1 < G and kg < G: group score = sum of the group's m largest scores
+ * (summed in ascending order, binary64); the G - kg groups with the lowest
+ * group score are banned (on equal score the higher index is banned first).
+ * The k best allowed experts are taken by (score desc, index asc).
+ * weight_mode: ORC_W_SOFTMAX_TOPK   softmax over the k selected scores,
+ *              ORC_W_SOFTMAX_RENORM softmax over all E, renormalised over the k,
+ *              ORC_W_SCORE_NORM     s_j / sum of the k selected s.
+ * Outputs topk_idx [T][k] int32 and topk_w [T][k] binary64. */
+int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k,
+              int weight_mode, int32_t* topk_idx, double* topk_w);
+
+/* Per-expert counting and prefix layout of the (token, j) pairs.
+ * topk_idx [T][k]: -1 = masked (no row); ids outside [-1, E) or an expert
+ * repeated within a token are invalid: the pair gets no row and the call
+ * returns ORC_ERR_INVALID.
+ * Outputs: cnt [E], off [E+1] (exclusive prefix of cnt), rcnt [R] (sum of the
+ * L = E/R experts of rank r), roff [R+1], row [T][k]:
+ *   HT: row = off[e] + (number of earlier pairs (t', j') < (t, j) with expert e)
+ *   LL: row = e * S + that same in-expert rank (slot), slot < S else overflow. */
+int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
+               int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row);
+
+/* Dispatch: every (t, j) with row r >= 0 receives token t.
+ * fp8 == 0: recv_x is bf16 [nrows][H] and recv_scale is unused.
+ * fp8 != 0: recv_x is e4m3 [nrows][H], recv_scale fp32 [nrows][H/128].
+ * recv_src [nrows] int32 gets t.  Rows never named by row[] are not touched. */
+int orc_dispatch(const uint16_t* x, int64_t T, int H, int k, const int32_t* row, int64_t nrows,
+                 int fp8, void* recv_x, float* recv_scale, int32_t* recv_src);
+
+/* Combine: out[t] = bf16_rn( sum_j w[t][j] * y[row[t][j]] ), accumulated in
+ * binary64 in j order; masked pairs (row < 0) contribute nothing.
+ * tokens == NULL: all T tokens, out is [T][H]; otherwise the ntok listed tokens,
+ * out is [ntok][H]. */
+int orc_combine(const uint16_t* y, int64_t nrows, int H, const int32_t* row, const float* w,
+                int64_t T, int k, const int64_t* tokens, int64_t ntok, uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
