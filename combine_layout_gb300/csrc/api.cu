@@ -1,0 +1,377 @@
+// C ABI of libmoeep: groups, handles, argument checks and kernel launches.
+// The operations follow "NCCL EP 论文解读", item "核心功能函数" (group, handle,
+// dispatch, combine, receive-count query); see include/moe_ep.h for the
+// contract of every call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+
+using namespace moeep;
+
+struct moe_ep_group {
+    int mode, E, R, L, S, H;
+    int device, sm_count;
+    int handles;                  // live handles
+    volatile unsigned* err_host;  // [kErrSlots], mapped pinned memory
+    unsigned* err_dev;            // device alias of err_host
+};
+
+struct moe_ep_handle {
+    moe_ep_group* g;
+    int max_topk;
+    int ntiles_max;
+    // device workspace
+    uint32_t* tile_word;  // [ntiles_max][E]
+    int32_t* tile_base;   // [ntiles_max][E]
+    int32_t* cnt;         // [E]
+    int32_t* off;         // [E+1]
+    int32_t* rcnt;        // [R]
+    int32_t* roff;        // [R+1]
+    int32_t* row;         // [max_tokens * max_topk]
+    // pinned host staging for the receive-count query: off[E+1] then rcnt[R]
+    int32_t* host_stage;
+    // state of the last route
+    int routed;
+    int T, k;
+    int64_t host_total;  // total rows known on the host (-1: not queried)
+};
+
+namespace {
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_EP_OK : MOE_EP_ERR_CUDA; }
+
+inline int check_group(const moe_ep_group* g)
+{
+    if (!g) return MOE_EP_ERR_INVALID;
+    for (int i = 0; i < kErrSlots; ++i)
+        if (g->err_host[i]) return MOE_EP_ERR_DEVICE;
+    return MOE_EP_OK;
+}
+
+// Next 256-byte-aligned piece of a handle's single device allocation.
+template <typename T>
+T* carve(char*& cur, size_t count)
+{
+    T* p = reinterpret_cast<T*>(cur);
+    size_t bytes = (sizeof(T) * count + 255) & ~(size_t)255;
+    cur += bytes;
+    return p;
+}
+
+int64_t required_rows(const moe_ep_handle* h)
+{
+    const moe_ep_group* g = h->g;
+    if (g->mode == MOE_EP_LL) return (int64_t)g->E * g->S;
+    if (h->host_total >= 0) return h->host_total;
+    return (int64_t)h->T * h->k;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_ep_status_string(int status)
+{
+    switch (status) {
+        case MOE_EP_OK: return "ok";
+        case MOE_EP_ERR_INVALID: return "invalid argument";
+        case MOE_EP_ERR_OVERFLOW: return "more tokens than max_tokens";
+        case MOE_EP_ERR_CUDA: return "CUDA runtime error";
+        case MOE_EP_ERR_DEVICE: return "device-error word set";
+        default: return "unknown status";
+    }
+}
+
+int moe_ep_create_group(moe_ep_group_t* out, int mode, int experts, int ranks, int max_tokens,
+                        int hidden)
+{
+    if (!out) return MOE_EP_ERR_INVALID;
+    *out = nullptr;
+    if (mode != MOE_EP_LL && mode != MOE_EP_HT) return MOE_EP_ERR_INVALID;
+    if (experts < 1 || experts > kMaxExperts || ranks < 1 || experts % ranks != 0)
+        return MOE_EP_ERR_INVALID;
+    if (max_tokens < 1 || hidden < 8 || hidden % 8 != 0) return MOE_EP_ERR_INVALID;
+    // row ids are int32: every receive row index must fit
+    if ((int64_t)experts * max_tokens > INT32_MAX || (int64_t)max_tokens * kMaxTopk > INT32_MAX)
+        return MOE_EP_ERR_INVALID;
+
+    moe_ep_group* g = new (std::nothrow) moe_ep_group();
+    if (!g) return MOE_EP_ERR_INVALID;
+    g->mode = mode;
+    g->E = experts;
+    g->R = ranks;
+    g->L = experts / ranks;
+    g->S = max_tokens;
+    g->H = hidden;
+    if (cudaGetDevice(&g->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device) !=
+            cudaSuccess) {
+        delete g;
+        return MOE_EP_ERR_CUDA;
+    }
+    void* hp = nullptr;
+    if (cudaHostAlloc(&hp, sizeof(unsigned) * kErrSlots, cudaHostAllocMapped) != cudaSuccess) {
+        delete g;
+        return MOE_EP_ERR_CUDA;
+    }
+    memset(hp, 0, sizeof(unsigned) * kErrSlots);
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess) {
+        cudaFreeHost(hp);
+        delete g;
+        return MOE_EP_ERR_CUDA;
+    }
+    g->err_host = (volatile unsigned*)hp;
+    g->err_dev = (unsigned*)dp;
+    *out = g;
+    return MOE_EP_OK;
+}
+
+int moe_ep_destroy_group(moe_ep_group_t g)
+{
+    if (!g) return MOE_EP_ERR_INVALID;
+    if (g->handles != 0) return MOE_EP_ERR_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFreeHost((void*)g->err_host);
+    delete g;
+    return cuda_status(e);
+}
+
+int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
+{
+    if (!g || !out || max_topk < 1 || max_topk > kMaxTopk || max_topk > g->E)
+        return MOE_EP_ERR_INVALID;
+    *out = nullptr;
+    moe_ep_handle* h = new (std::nothrow) moe_ep_handle();
+    if (!h) return MOE_EP_ERR_INVALID;
+    h->g = g;
+    h->max_topk = max_topk;
+    h->ntiles_max = (g->S + kTileTokens - 1) / kTileTokens;
+    const size_t nt = (size_t)h->ntiles_max * g->E;
+    // one allocation, carved in this order, each piece 256-byte aligned
+    const size_t counts[7] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+                              (size_t)g->R + 1, (size_t)g->S * max_topk};
+    size_t bytes = 0;
+    for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
+    void* base = nullptr;
+    if (cudaMalloc(&base, bytes) != cudaSuccess) {
+        delete h;
+        return MOE_EP_ERR_CUDA;
+    }
+    char* cur = (char*)base;
+    h->tile_word = carve<uint32_t>(cur, counts[0]);
+    h->tile_base = carve<int32_t>(cur, counts[1]);
+    h->cnt = carve<int32_t>(cur, counts[2]);
+    h->off = carve<int32_t>(cur, counts[3]);
+    h->rcnt = carve<int32_t>(cur, counts[4]);
+    h->roff = carve<int32_t>(cur, counts[5]);
+    h->row = carve<int32_t>(cur, counts[6]);
+    void* hs = nullptr;
+    if (cudaHostAlloc(&hs, sizeof(int32_t) * (size_t)(g->E + 1 + g->R), cudaHostAllocDefault) !=
+        cudaSuccess) {
+        cudaFree(base);
+        delete h;
+        return MOE_EP_ERR_CUDA;
+    }
+    h->host_stage = (int32_t*)hs;
+    h->routed = 0;
+    h->host_total = -1;
+    g->handles += 1;
+    *out = h;
+    return MOE_EP_OK;
+}
+
+int moe_ep_destroy_handle(moe_ep_handle_t h)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(h->tile_word);  // start of the single allocation
+    cudaFreeHost(h->host_stage);
+    h->g->handles -= 1;
+    delete h;
+    return cuda_status(e);
+}
+
+int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
+                 const moe_ep_route_opts_t* opts, int32_t* topk_idx, float* topk_w,
+                 moe_ep_stream_t stream)
+{
+    if (!h || !opts) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    const int T = num_tokens, k = opts->topk;
+    if (T < 0 || k < 1 || k > h->max_topk || k > g->E) return MOE_EP_ERR_INVALID;
+    if (T > g->S) return MOE_EP_ERR_OVERFLOW;
+    if (T > 0 && !topk_idx) return MOE_EP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+
+    if (scores) {
+        RouteParams p;
+        p.E = g->E;
+        p.G = opts->num_groups;
+        p.kg = opts->topk_groups;
+        p.k = k;
+        p.wmode = opts->weight_mode;
+        if (p.G < 1 || p.G > kMaxGroups || g->E % p.G != 0) return MOE_EP_ERR_INVALID;
+        if (p.kg < 1 || p.kg > p.G) return MOE_EP_ERR_INVALID;
+        if (p.wmode < MOE_EP_W_SOFTMAX_TOPK || p.wmode > MOE_EP_W_SCORE_NORM) return MOE_EP_ERR_INVALID;
+        p.gs = g->E / p.G;
+        if ((int64_t)p.kg * p.gs < k) return MOE_EP_ERR_INVALID;
+        p.limit = (p.G > 1 && p.kg < p.G) ? 1 : 0;
+        p.m = opts->group_topk > 0 ? opts->group_topk : (k + p.kg - 1) / p.kg;
+        if (p.limit && (p.m < 1 || p.m > kMaxGroupTopk || p.m > p.gs)) return MOE_EP_ERR_INVALID;
+        p.lpg = 1;
+        p.lpg_log2 = 0;
+        while (p.lpg * 2 * p.G <= 32) {
+            p.lpg *= 2;
+            p.lpg_log2 += 1;
+        }
+        p.epl = (p.gs + p.lpg - 1) / p.lpg;
+        if (p.epl > kMaxExpertsPerLane) return MOE_EP_ERR_INVALID;
+        st = cuda_status(launch_route(scores, T, p, topk_idx, topk_w, h->tile_word, s));
+    } else {
+        st = cuda_status(launch_layout_bits(topk_idx, T, k, g->E, h->tile_word, g->err_dev, s));
+    }
+    if (st != MOE_EP_OK) return st;
+    st = cuda_status(launch_layout_scan(h->tile_word, ntiles, g->E, h->tile_base, h->cnt, s));
+    if (st != MOE_EP_OK) return st;
+    st = cuda_status(launch_rowmap(topk_idx, T, k, g->E, g->R, g->mode, g->S, h->tile_word,
+                                   h->tile_base, h->cnt, h->off, h->rcnt, h->roff, h->row,
+                                   g->sm_count, s));
+    if (st != MOE_EP_OK) return st;
+    h->routed = 1;
+    h->T = T;
+    h->k = k;
+    h->host_total = -1;
+    return MOE_EP_OK;
+}
+
+int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_rank,
+                               int32_t* per_expert, moe_ep_stream_t stream)
+{
+    if (!h || !total) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    if (g->mode == MOE_EP_LL) {
+        *total = (int64_t)g->E * g->S;
+        if (per_rank)
+            for (int r = 0; r < g->R; ++r) per_rank[r] = g->L * g->S;
+        if (per_expert)
+            for (int e = 0; e < g->E; ++e) per_expert[e] = g->S;
+        return MOE_EP_OK;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(h->host_stage, h->off, sizeof(int32_t) * (size_t)(g->E + 1),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->host_stage + g->E + 1, h->rcnt, sizeof(int32_t) * (size_t)g->R,
+                            cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_EP_ERR_CUDA;
+    st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    const int32_t* off = h->host_stage;
+    *total = off[g->E];
+    h->host_total = off[g->E];
+    if (per_rank) memcpy(per_rank, h->host_stage + g->E + 1, sizeof(int32_t) * (size_t)g->R);
+    if (per_expert)
+        for (int x = 0; x < g->E; ++x) per_expert[x] = off[x + 1] - off[x];
+    return MOE_EP_OK;
+}
+
+int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, float* recv_scale,
+                    int32_t* recv_src, int32_t* recv_cnt, int64_t recv_rows,
+                    moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    if (recv_rows < required_rows(h)) return MOE_EP_ERR_INVALID;
+    if (h->T > 0 && (!x || !recv_x || !aligned16(x) || !aligned16(recv_x)))
+        return MOE_EP_ERR_INVALID;
+    if (fp8) {
+        if (g->H % 128 != 0) return MOE_EP_ERR_INVALID;
+        if (h->T > 0 && (!recv_scale || ((uintptr_t)recv_scale & 3u))) return MOE_EP_ERR_INVALID;
+    }
+    if (recv_src && ((uintptr_t)recv_src & 3u)) return MOE_EP_ERR_INVALID;
+    if (recv_cnt && ((uintptr_t)recv_cnt & 3u)) return MOE_EP_ERR_INVALID;
+    return cuda_status(launch_dispatch(x, h->T, g->H, h->k, fp8, h->row, recv_x, recv_scale,
+                                       recv_src, h->cnt, recv_cnt, g->E, g->sm_count,
+                                       (cudaStream_t)stream));
+}
+
+int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
+                   int64_t recv_rows, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    if (recv_rows < required_rows(h)) return MOE_EP_ERR_INVALID;
+    if (h->T > 0) {
+        if (!y || !topk_w || !out || !aligned16(y) || !aligned16(out) || ((uintptr_t)topk_w & 3u))
+            return MOE_EP_ERR_INVALID;
+        // out must not overlap y
+        const char* yb = (const char*)y;
+        const char* ye = yb + (size_t)recv_rows * g->H * 2;
+        const char* ob = (const char*)out;
+        const char* oe = ob + (size_t)h->T * g->H * 2;
+        if (ob < ye && yb < oe) return MOE_EP_ERR_INVALID;
+    }
+    return cuda_status(launch_combine(y, h->T, g->H, h->k, h->row, topk_w, out, g->sm_count,
+                                      (cudaStream_t)stream));
+}
+
+int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff,
+                       int32_t* row, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (cnt && e == cudaSuccess)
+        e = cudaMemcpyAsync(cnt, h->cnt, sizeof(int32_t) * g->E, cudaMemcpyDefault, s);
+    if (off && e == cudaSuccess)
+        e = cudaMemcpyAsync(off, h->off, sizeof(int32_t) * (g->E + 1), cudaMemcpyDefault, s);
+    if (rcnt && e == cudaSuccess)
+        e = cudaMemcpyAsync(rcnt, h->rcnt, sizeof(int32_t) * g->R, cudaMemcpyDefault, s);
+    if (roff && e == cudaSuccess)
+        e = cudaMemcpyAsync(roff, h->roff, sizeof(int32_t) * (g->R + 1), cudaMemcpyDefault, s);
+    if (row && e == cudaSuccess && h->T > 0)
+        e = cudaMemcpyAsync(row, h->row, sizeof(int32_t) * (size_t)h->T * h->k, cudaMemcpyDefault,
+                            s);
+    return cuda_status(e);
+}
+
+int moe_ep_get_device_errors(moe_ep_group_t g, uint32_t* bits)
+{
+    if (!g || !bits) return MOE_EP_ERR_INVALID;
+    uint32_t b = 0;
+    if (g->err_host[kErrRange]) b |= MOE_EP_DEVERR_EXPERT_RANGE;
+    if (g->err_host[kErrDuplicate]) b |= MOE_EP_DEVERR_DUPLICATE;
+    *bits = b;
+    return MOE_EP_OK;
+}
+
+int moe_ep_clear_device_errors(moe_ep_group_t g)
+{
+    if (!g) return MOE_EP_ERR_INVALID;
+    for (int i = 0; i < kErrSlots; ++i) g->err_host[i] = 0u;
+    return MOE_EP_OK;
+}
+
+}  // extern "C"

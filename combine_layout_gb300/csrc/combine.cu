@@ -1,0 +1,105 @@
+// Combine: gather each token's k expert-output rows back to token order and
+// reduce them with the gate weights.
+//
+// "NCCL EP 论文解读", item "核心功能函数": combine collects the tokens and reduces
+// them to the original order, un-permuting with the routing state stored in
+// the handle.  "NVSHMEM 与 DeepEP：GPU 发起的通信", section "高吞吐模式": what comes
+// back is the weighted sum of the expert outputs, kept in BF16.
+//
+// out[t][h] = bf16_rn(fma(w_{k-1}, y_{k-1}, ... fma(w_1, y_1, fma(w_0, y_0, 0)))),
+// fp32 accumulation in fixed j order, so results do not depend on scheduling.
+// HBM-bound: k gathered row reads and one row write per token; every thread
+// issues the loads of all k rows for its 16-byte slice before accumulating.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moeep {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ void acc8(float (&a)[8], float w, const uint4& v)
+{
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), a[2 * i]);
+        a[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xffff0000u), a[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8])
+{
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint4* __restrict__ y, int T, int k, int nvec, const int32_t* __restrict__ row,
+    const float* __restrict__ w, uint4* __restrict__ out)
+{
+    __shared__ int s_row[KMAX];
+    __shared__ float s_w[KMAX];
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x < k) {
+            s_row[threadIdx.x] = row[(size_t)t * k + threadIdx.x];
+            s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+        }
+        __syncthreads();
+        int r[KMAX];
+        float wj[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            r[j] = j < k ? s_row[j] : -1;
+            wj[j] = j < k ? s_w[j] : 0.f;
+        }
+        for (int v = threadIdx.x; v < nvec; v += kThreads) {
+            uint4 val[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (r[j] >= 0) val[j] = __ldg(y + (size_t)r[j] * nvec + v);
+            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (r[j] >= 0) acc8(a, wj[j], val[j]);
+            out[(size_t)t * nvec + v] = pack8(a);
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,
+                           void* out, int sm_count, cudaStream_t s)
+{
+    if (T <= 0) return cudaSuccess;
+    const int nvec = H / 8;
+    int blocks = T;
+    const int cap = sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    const uint4* yy = (const uint4*)y;
+    uint4* oo = (uint4*)out;
+    if (k <= 1)
+        combine_kernel<1><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    else if (k <= 2)
+        combine_kernel<2><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    else if (k <= 4)
+        combine_kernel<4><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    else if (k <= 8)
+        combine_kernel<8><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    else if (k <= 16)
+        combine_kernel<16><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    else
+        combine_kernel<32><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
+    return cudaGetLastError();
+}
+
+}  // namespace moeep

@@ -1,0 +1,94 @@
+"""One group + one handle with their receive buffers (torch device memory).
+
+Allocation and argument marshalling only: every step runs in libmoeep's
+kernels through the C ABI (``moe_ep``).  The order of calls is the one on
+"NCCL EP 论文解读", item "使用方式": create the group once, then per forward
+route -> (HT: receive-count query) -> dispatch -> experts -> combine.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import moe_ep as ep
+
+
+class EpPipeline:
+    def __init__(self, mode: int, experts: int, ranks: int, max_tokens: int, hidden: int,
+                 topk: int, fp8: bool = False, device: str | int = "cuda"):
+        self.mode, self.E, self.R, self.S, self.H, self.k = mode, experts, ranks, max_tokens, hidden, topk
+        self.fp8 = fp8
+        self.device = torch.device(device)
+        self.group = ep.moe_ep_create_group(mode, experts, ranks, max_tokens, hidden)
+        self.handle = ep.moe_ep_create_handle(self.group, topk)
+        self.rows = experts * max_tokens if mode == ep.MOE_EP_LL else max_tokens * topk
+        dev = self.device
+        self.topk_idx = torch.empty((max_tokens, topk), dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty((max_tokens, topk), dtype=torch.float32, device=dev)
+        self.recv_x = torch.empty((self.rows, hidden), dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                  device=dev)
+        self.recv_scale = (torch.empty((self.rows, hidden // 128), dtype=torch.float32, device=dev)
+                           if fp8 else None)
+        self.recv_src = torch.empty(self.rows, dtype=torch.int32, device=dev)
+        self.recv_cnt = torch.empty(experts, dtype=torch.int32, device=dev)
+        self.out = torch.empty((max_tokens, hidden), dtype=torch.bfloat16, device=dev)
+        self.T = 0
+
+    # ---------------------------------------------------------------- steps
+    def route(self, scores, num_tokens: int, num_groups: int = 1, topk_groups: int = 1,
+              group_topk: int = 0, weight_mode: int = ep.MOE_EP_W_SCORE_NORM, stream=None):
+        self.T = num_tokens
+        ep.moe_ep_route(self.handle, scores, num_tokens, self.k, self.topk_idx, self.topk_w,
+                        num_groups, topk_groups, group_topk, weight_mode, stream)
+
+    def route_given(self, topk_idx, stream=None):
+        """Lay out caller-made routing (topk_idx [T][k] int32 on the device)."""
+        T = topk_idx.shape[0]
+        self.topk_idx[:T].copy_(topk_idx)
+        self.T = T
+        ep.moe_ep_route(self.handle, None, T, self.k, self.topk_idx, None, stream=stream)
+
+    def num_recv_tokens(self, stream=None):
+        return ep.moe_ep_get_num_recv_tokens(self.handle, self.R, self.E, stream)
+
+    def dispatch(self, x, stream=None):
+        ep.moe_ep_dispatch(self.handle, x, self.fp8, self.recv_x, self.recv_scale, self.recv_src,
+                           self.recv_cnt, self.rows, stream)
+
+    def combine(self, y, topk_w=None, out=None, stream=None):
+        if topk_w is None:
+            topk_w = self.topk_w
+        if out is None:
+            out = self.out
+        ep.moe_ep_combine(self.handle, y, topk_w, out, y.shape[0], stream)
+        return out[: self.T]
+
+    def layout(self, stream=None) -> dict:
+        dev = self.device
+        L = dict(cnt=torch.empty(self.E, dtype=torch.int32, device=dev),
+                 off=torch.empty(self.E + 1, dtype=torch.int32, device=dev),
+                 rcnt=torch.empty(self.R, dtype=torch.int32, device=dev),
+                 roff=torch.empty(self.R + 1, dtype=torch.int32, device=dev),
+                 row=torch.empty((max(self.T, 1), self.k), dtype=torch.int32, device=dev))
+        ep.moe_ep_copy_layout(self.handle, L["cnt"], L["off"], L["rcnt"], L["roff"], L["row"], stream)
+        L["row"] = L["row"][: self.T]
+        return L
+
+    def device_errors(self) -> int:
+        return ep.moe_ep_get_device_errors(self.group)
+
+    def clear_device_errors(self):
+        ep.moe_ep_clear_device_errors(self.group)
+
+    def close(self):
+        if self.handle:
+            ep.moe_ep_destroy_handle(self.handle)
+            self.handle = None
+        if self.group:
+            ep.moe_ep_destroy_group(self.group)
+            self.group = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,196 @@
+/*
+ * moe_ep.h -- C ABI of libmoeep: MoE expert-parallel token dispatch and combine
+ * on one GPU (sm_103a), destination ranks being logical partitions of the GPU's
+ * own memory.
+ *
+ * The calls follow the statement of the problem on "NCCL EP 论文解读" (lpnh.cn),
+ * item "核心功能函数": a group holds the resources shared across operations, a
+ * handle holds one forward pass's routing state created from topk_idx, dispatch
+ * sends tokens to their experts, combine gathers them back into the original
+ * token order and reduces them, and a receive-count query serves buffer sizing.
+ * The two algorithm modes are those of item "算法模式" and of
+ * "NVSHMEM 与 DeepEP：GPU 发起的通信" (anrans.github.io), sections "高吞吐模式" (HT)
+ * and "低延迟模式" (LL).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" must point to memory the current CUDA device can
+ *    access; "host" pointers are ordinary host memory.  The caller owns every
+ *    buffer passed in or out; the library owns only the workspace of groups
+ *    and handles, allocated once at creation (nothing is allocated per call).
+ *  - Every call is asynchronous on the given stream except where stated.  A
+ *    NULL stream is the legacy default stream.
+ *  - bf16 buffers are passed as void* holding IEEE bfloat16 bit patterns;
+ *    fp8 buffers hold OCP e4m3fn bytes.  All integers are int32 unless stated.
+ *  - Every call returns a moe_ep_status_t.  Argument and capacity errors are
+ *    found on the host before any launch.  Invalid data found on the device
+ *    (an expert id out of range, an expert repeated within a token) never
+ *    causes an out-of-bounds access: the pair is dropped and a bit is latched
+ *    in the group's device-error word, which is visible to the host without a
+ *    synchronisation once the kernel has finished; while it is set every call
+ *    on the group returns MOE_EP_ERR_DEVICE until moe_ep_clear_device_errors.
+ *    Kernels never trap and never wait on another kernel.
+ *  - A handle's workspace is reused by each moe_ep_route call: use one handle
+ *    per forward pass in flight (for instance one per layer).
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_EP_API __attribute__((visibility("default")))
+#else
+#define MOE_EP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* moe_ep_stream_t;
+
+typedef enum {
+    MOE_EP_LL = 0, /* low latency: fixed worst-case slots, no count exchange */
+    MOE_EP_HT = 1  /* high throughput: dense 2D receive layout, counts known after one sync */
+} moe_ep_mode_t;
+
+typedef enum {
+    MOE_EP_OK = 0,
+    MOE_EP_ERR_INVALID = 1,  /* bad argument, shape or alignment */
+    MOE_EP_ERR_OVERFLOW = 2, /* more tokens than the group's max_tokens (LL slots) */
+    MOE_EP_ERR_CUDA = 3,     /* a CUDA runtime call or launch failed */
+    MOE_EP_ERR_DEVICE = 4    /* device-error word set (see moe_ep_get_device_errors) */
+} moe_ep_status_t;
+
+/* Bits of the device-error word. */
+#define MOE_EP_DEVERR_EXPERT_RANGE 1u /* a topk_idx entry outside [-1, experts) */
+#define MOE_EP_DEVERR_DUPLICATE 2u    /* an expert repeated within one token */
+
+typedef enum {
+    MOE_EP_W_SOFTMAX_TOPK = 0,   /* w_j = softmax over the k selected scores */
+    MOE_EP_W_SOFTMAX_RENORM = 1, /* softmax over all experts, renormalised over the k */
+    MOE_EP_W_SCORE_NORM = 2      /* w_j = s_j / sum of the k selected scores */
+} moe_ep_weight_mode_t;
+
+typedef struct moe_ep_group* moe_ep_group_t;
+typedef struct moe_ep_handle* moe_ep_handle_t;
+
+/* Routing options ("NVSHMEM 与 DeepEP：GPU 发起的通信", section "高吞吐模式": keep the
+ * best topk_groups nodes by the sum of each node's group_topk best expert
+ * scores, then take the topk best experts among them). */
+typedef struct {
+    int topk;        /* k, experts per token, 1..32 */
+    int num_groups;  /* G, routing groups (nodes); experts split into G contiguous blocks; 1 = no limit */
+    int topk_groups; /* groups kept per token, 1..G */
+    int group_topk;  /* scores summed per group, 1..4; 0 = ceil(topk / topk_groups) */
+    int weight_mode; /* moe_ep_weight_mode_t */
+} moe_ep_route_opts_t;
+
+/* Create a communication group ("核心功能函数": ncclEpCreateGroup picks the
+ * algorithm mode, the expert count, the maximum tokens per rank and the buffer
+ * sizes).  experts E are split over `ranks` R logical ranks in contiguous blocks
+ * of L = E / R ("Moe模型": E experts placed blockwise over N ranks); rank r
+ * belongs to no physical device other than the current one.  max_tokens bounds
+ * the tokens of one forward; in LL mode it is also the slot count S per
+ * (rank, local expert) ("低延迟模式": num_max_dispatch_tokens_per_rank).
+ * hidden H is the token width in elements, a multiple of 8 (128 for FP8).
+ * Synchronous.  Allocates the group's device-error word on the current device.
+ * Errors: MOE_EP_ERR_INVALID for E % R != 0, E > 512, non-positive sizes,
+ * H % 8 != 0; MOE_EP_ERR_CUDA if the device cannot be queried or allocated. */
+MOE_EP_API int moe_ep_create_group(moe_ep_group_t* out, int mode, int experts, int ranks, int max_tokens,
+                        int hidden);
+/* Frees the group.  Its handles must have been destroyed first
+ * (MOE_EP_ERR_INVALID otherwise).  Synchronous (waits for the device). */
+MOE_EP_API int moe_ep_destroy_group(moe_ep_group_t g);
+
+/* Create a routing handle ("核心功能函数": ncclEpCreateHandle, one per forward
+ * pass, shared by the matching dispatch and combine).  Allocates, once, the
+ * device workspace for max_tokens x max_topk pairs: per-tile expert bitmaps,
+ * column prefixes, counts, offsets and the row map.  Synchronous. */
+MOE_EP_API int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out);
+MOE_EP_API int moe_ep_destroy_handle(moe_ep_handle_t h);
+
+/* Route num_tokens tokens and lay out their (token, j) pairs.
+ * scores   device fp32 [T][E] row-major, or NULL: then topk_idx is an input
+ *          (routing made by the caller) and topk_w is not touched.
+ * topk_idx device int32 [T][k]: output (or input when scores == NULL).  Row t
+ *          lists token t's experts best first (score descending, lower index
+ *          on ties).  As an input, -1 masks a pair (it gets no row).
+ * topk_w   device fp32 [T][k], output weights per opts->weight_mode; may be NULL.
+ * Layout (HT): expert e's pairs occupy receive rows [off[e], off[e+1]) in
+ * ascending token order, i.e. rows are ordered by (rank, local expert, token)
+ * ("算法模式": deterministic order, per-expert counts mark the boundaries).
+ * Layout (LL): pair (t, j) with expert e = r * L + l goes to slot
+ * s = #(earlier tokens of e) of row e * S + s, i.e. [r][l][s] of the
+ * [R][L][S][H] receive buffer ("Tensor Layouts": 3D expert-major).
+ * Errors: MOE_EP_ERR_OVERFLOW if num_tokens > max_tokens; MOE_EP_ERR_INVALID
+ * for bad options (k > max_topk, E % G, G > 32, kg * E / G < k, ...). */
+MOE_EP_API int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
+                 const moe_ep_route_opts_t* opts, int32_t* topk_idx, float* topk_w,
+                 moe_ep_stream_t stream);
+
+/* Receive-token query ("核心功能函数": ncclEpHandleGetNumRecvTokens, used for
+ * buffer sizing).  HT: copies the total receive rows and, if non-NULL, the
+ * per-rank [R] and per-expert [E] counts to the host -- the one host
+ * synchronisation of HT mode ("高吞吐模式": the CPU must learn the receive size);
+ * it synchronises `stream`.  LL: returns the fixed capacity without any
+ * synchronisation ("低延迟模式": no count exchange): total = E * S,
+ * per_rank[r] = L * S, per_expert[e] = S.
+ * total, per_rank, per_expert: host pointers (per_rank/per_expert may be NULL). */
+MOE_EP_API int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_rank,
+                               int32_t* per_expert, moe_ep_stream_t stream);
+
+/* Dispatch ("核心功能函数": ncclEpDispatch; "通信模式": read the token, write it to
+ * the buffer, quantise in-kernel when FP8 is on).  Every pair with a row gets a
+ * copy of its token.
+ * x          device bf16 [T][H] (16-byte aligned).
+ * fp8 == 0:  recv_x device bf16 [recv_rows][H]; recv_scale unused (may be NULL).
+ * fp8 != 0:  recv_x device e4m3 [recv_rows][H]; recv_scale device fp32
+ *            [recv_rows][H/128]: per block of 128 elements of one token,
+ *            scale = amax / 448 (1 when amax == 0) and q = e4m3(x / scale),
+ *            IEEE fp32 division, round to nearest even, saturating
+ *            ("高吞吐模式": FP8 with one scale per 128 elements).
+ * recv_src   device int32 [recv_rows] or NULL: source token of each written row.
+ * recv_cnt   device int32 [E] or NULL: per-expert receive counts
+ *            ("Tensor Layouts": _RECV_EXPERT_COUNTER_DEVICE).
+ * recv_rows  rows the receive buffers hold: at least T * k (HT; or the total of
+ *            the last moe_ep_get_num_recv_tokens) or E * S (LL).  Rows not
+ *            named by the layout are left untouched (LL's unused slots are
+ *            never cleared).
+ * Errors: MOE_EP_ERR_INVALID for misaligned pointers, H % 128 != 0 with fp8,
+ * recv_rows too small, or no preceding moe_ep_route on the handle. */
+MOE_EP_API int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, float* recv_scale,
+                    int32_t* recv_src, int32_t* recv_cnt, int64_t recv_rows,
+                    moe_ep_stream_t stream);
+
+/* Combine ("核心功能函数": ncclEpCombine gathers the tokens back and reduces them
+ * to the original order using the handle's routing state; "高吞吐模式": the
+ * result is the BF16 weighted sum of the expert outputs).
+ * out[t][h] = bf16_rn( sum over j = 0..k-1 with a row of w[t][j] * y[row(t,j)][h] ),
+ * an fp32 fused multiply-add chain in j order, rounded once to nearest even.
+ * y       device bf16 in the receive layout [recv_rows][H] (16-byte aligned).
+ * topk_w  device fp32 [T][k].
+ * out     device bf16 [T][H] (16-byte aligned); must not overlap y.
+ * Errors as for dispatch. */
+MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
+                   int64_t recv_rows, moe_ep_stream_t stream);
+
+/* Copy the handle's layout to caller buffers (device or host pointers; NULL
+ * skips an item): cnt [E], off [E+1], rcnt [R], roff [R+1], row [T][k] with -1
+ * for pairs without a row.  Asynchronous for device destinations; host
+ * destinations must be pinned for the copy to be asynchronous. */
+MOE_EP_API int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* rcnt,
+                       int32_t* roff, int32_t* row, moe_ep_stream_t stream);
+
+/* Read (host, no synchronisation) / clear the group's device-error word. */
+MOE_EP_API int moe_ep_get_device_errors(moe_ep_group_t g, uint32_t* bits);
+MOE_EP_API int moe_ep_clear_device_errors(moe_ep_group_t g);
+
+/* Static description of a status code. */
+MOE_EP_API const char* moe_ep_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

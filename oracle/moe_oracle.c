@@ -171,10 +171,15 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
     double* tmp = (double*)malloc(sizeof(double) * (size_t)gs);
     scored* nodes = (scored*)malloc(sizeof(scored) * (size_t)G);
     scored* cand = (scored*)malloc(sizeof(scored) * (size_t)E);
+    float* sv = (float*)malloc(sizeof(float) * (size_t)E);
 
     for (int64_t t = 0; t < T; ++t) {
-        const float* s = scores + t * E;
-        for (int e = 0; e < E; ++e) allowed[e] = 1;
+        const float* s_in = scores + t * E;
+        for (int e = 0; e < E; ++e) {
+            allowed[e] = 1;
+            sv[e] = isnan(s_in[e]) ? -INFINITY : s_in[e];   /* NaN ranks as -infinity */
+        }
+        const float* s = sv;
 
         /* Step 1 (node limit): score every node by the sum of its m best
          * expert scores, then ban the G - kg lowest-scoring nodes. */
@@ -221,7 +226,7 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
             for (int j = 0; j < k; ++j) w[j] = w[j] / sel;
         }
     }
-    free(allowed); free(tmp); free(nodes); free(cand);
+    free(allowed); free(tmp); free(nodes); free(cand); free(sv);
     return ORC_OK;
 }
 

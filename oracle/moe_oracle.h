@@ -54,6 +54,7 @@ int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale);
  * (summed in ascending order, binary64); the G - kg groups with the lowest
  * group score are banned (on equal score the higher index is banned first).
  * The k best allowed experts are taken by (score desc, index asc).
+ * A NaN score ranks as -infinity.
  * weight_mode: ORC_W_SOFTMAX_TOPK   softmax over the k selected scores,
  *              ORC_W_SOFTMAX_RENORM softmax over all E, renormalised over the k,
  *              ORC_W_SCORE_NORM     s_j / sum of the k selected s.

@@ -1,0 +1,60 @@
+"""Shared helpers for the GPU-vs-oracle parity tests (test code only).
+
+Tolerances, derived from the arithmetic:
+  - routing indices, counts, offsets, row map, receive rows, FP8 bytes and
+    scales, source ids: bit-exact (integer / byte work, and the FP8 code is
+    decided by one fp32 division on both sides).
+  - gate weights: the kernel computes in fp32, the oracle in binary64.  A sum
+    of k <= 8 positive fp32 terms plus one division is within (k+1) units of
+    2^-24 relative; softmax adds expf's error (<= 2 ulp) and one more
+    division.  Bound used: 32 * 2^-24 relative (~1.9e-6).
+  - combine: the kernel accumulates k fp32 fused multiply-adds and rounds once
+    to bf16; the oracle sums exactly-representable products in binary64 and
+    rounds once.  The fp32 error (< k * 2^-24 relative) can move the result
+    across at most one bf16 rounding boundary: <= 1 bf16 ulp.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from combine_layout_gb300 import synth
+
+W_RTOL = 32 * 2.0 ** -24
+
+
+def to_dev_bf16(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def defined_rows(w_mode: int, cnt: np.ndarray, S: int, total: int) -> np.ndarray:
+    """Receive rows the layout defines: HT [0, total); LL e*S + [0, cnt[e])."""
+    if w_mode == synth.MODE_HT:
+        return np.arange(total)
+    return np.concatenate([e * S + np.arange(c) for e, c in enumerate(cnt)]) if len(cnt) else \
+        np.zeros(0, np.int64)
+
+
+def dequant_on_device(q: torch.Tensor, scale: torch.Tensor, chunk: int = 8192) -> torch.Tensor:
+    """Identity expert for FP8 payloads (test harness, torch ops):
+    y = bf16(float(q) * scale) in the receive layout.  Any deterministic bf16 y
+    serves: the same y feeds the kernel and the oracle."""
+    rows, H = q.shape
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device=q.device)
+    for a in range(0, rows, chunk):
+        b = min(rows, a + chunk)
+        f = q[a:b].view(torch.float8_e4m3fn).float().view(b - a, H // 128, 128)
+        f = torch.nan_to_num(f * scale[a:b, :, None], nan=0.0, posinf=0.0, neginf=0.0)
+        y[a:b] = f.view(b - a, H).to(torch.bfloat16)
+    return y

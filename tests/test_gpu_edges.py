@@ -1,0 +1,209 @@
+"""GPU edge cases and error behaviour of the C ABI: empty and single-token
+batches, the maximum token count, masked and invalid expert ids (device-error
+word, no out-of-bounds writes), host-side argument checks, hot experts."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_layout_gb300 import synth
+from parity import bf16_bits, bf16_ulp_diff, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+def _ep():
+    import combine_layout_gb300.moe_ep as ep
+    return ep
+
+
+def _pipe(mode, E, R, S, H, k, fp8=False):
+    from combine_layout_gb300.pipeline import EpPipeline
+    return EpPipeline(mode, E, R, S, H, k, fp8=fp8, device=DEV)
+
+
+def test_empty_batch():
+    p = _pipe(synth.MODE_HT, 16, 4, 64, 256, 2)
+    scores = torch.zeros((0, 16), device=DEV)
+    p.route(scores, 0)
+    total, pr, pe = p.num_recv_tokens()
+    assert total == 0 and sum(pr) == 0 and sum(pe) == 0
+    p.dispatch(torch.zeros((1, 256), dtype=torch.bfloat16, device=DEV))
+    p.combine(p.recv_x)
+    torch.cuda.synchronize()
+    assert p.layout()["off"].cpu().tolist() == [0] * 17
+    p.close()
+
+
+@pytest.mark.parametrize("mode", [synth.MODE_LL, synth.MODE_HT])
+def test_single_token_and_max_tokens(mode):
+    E, R, S, H, k = 64, 8, 96, 512, 6
+    rng = np.random.default_rng(0)
+    for T in (1, S):
+        s = rng.random((T, E)).astype(np.float32)
+        x = synth.tokens_bf16(rng, T, H)
+        p = _pipe(mode, E, R, S, H, k)
+        p.route(torch.from_numpy(s).to(DEV), T, 8, 3)
+        p.dispatch(to_dev_bf16(x, DEV))
+        out = p.combine(p.recv_x)
+        torch.cuda.synchronize()
+        idx_o, _ = oracle.route(s, k, 8, 3)
+        assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
+        L_o, _ = oracle.layout(idx_o, E, R, mode, S)
+        assert np.array_equal(p.layout()["row"].cpu().numpy(), L_o["row"])
+        assert bf16_ulp_diff(bf16_bits(out), x).max() <= 1
+        p.close()
+
+
+def test_too_many_tokens_is_overflow():
+    ep = _ep()
+    p = _pipe(synth.MODE_LL, 16, 4, 32, 256, 2)
+    with pytest.raises(ep.MoeEpError) as e:
+        p.route(torch.zeros((33, 16), device=DEV), 33)
+    assert e.value.status == ep.MOE_EP_ERR_OVERFLOW
+    p.close()
+
+
+def test_masked_pairs_get_no_row_and_no_term():
+    T, E, R, H, k = 70, 8, 4, 256, 3
+    rng = np.random.default_rng(1)
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    idx[::5, 1] = -1
+    idx[7, :] = -1
+    x = synth.tokens_bf16(rng, T, H)
+    p = _pipe(synth.MODE_HT, E, R, T, H, k)
+    p.route_given(torch.from_numpy(idx).to(DEV))
+    total, _, _ = p.num_recv_tokens()
+    L_o, st = oracle.layout(idx, E, R, oracle.MODE_HT)
+    assert st == oracle.OK and total == int((idx >= 0).sum())
+    assert np.array_equal(p.layout()["row"].cpu().numpy(), L_o["row"])
+    p.dispatch(to_dev_bf16(x, DEV))
+    w = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(DEV)
+    out = p.combine(p.recv_x, w)
+    torch.cuda.synchronize()
+    want = oracle.combine(bf16_bits(p.recv_x), L_o["row"], w.cpu().numpy())
+    assert bf16_ulp_diff(bf16_bits(out), want).max() <= 1
+    assert np.all(bf16_bits(out)[7] == 0)
+    assert p.device_errors() == 0
+    p.close()
+
+
+def test_receive_buffer_sized_by_query():
+    """HT buffers sized exactly by the receive-count query are accepted."""
+    ep = _ep()
+    T, E, R, H, k = 64, 8, 4, 128, 2
+    idx = np.tile(np.array([[0, -1]], np.int32), (T, 1))
+    p = _pipe(synth.MODE_HT, E, R, T, H, k)
+    p.route_given(torch.from_numpy(idx).to(DEV))
+    x = torch.ones((T, H), dtype=torch.bfloat16, device=DEV)
+    small = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ep.MoeEpError):          # T*k rows required before the query
+        ep.moe_ep_dispatch(p.handle, x, False, small)
+    total, _, _ = p.num_recv_tokens()
+    assert total == T
+    ep.moe_ep_dispatch(p.handle, x, False, small)
+    torch.cuda.synchronize()
+    assert torch.equal(small, x)
+    p.close()
+
+
+def test_invalid_expert_ids_latch_device_error_without_stray_writes():
+    ep = _ep()
+    T, E, R, H, k = 40, 8, 4, 128, 2
+    idx = np.array([[t % E, (t + 1) % E] for t in range(T)], np.int32)
+    idx[3, 0] = 8          # out of range
+    idx[9, 1] = -7         # out of range
+    idx[12, 1] = idx[12, 0]  # repeated expert
+    p = _pipe(synth.MODE_HT, E, R, T, H, k)
+    guard = torch.full((p.rows + 64, H), 7, dtype=torch.bfloat16, device=DEV)
+    p.recv_x = guard[: p.rows]
+    p.route_given(torch.from_numpy(idx).to(DEV))
+    torch.cuda.synchronize()
+    bits = p.device_errors()
+    assert bits & ep.MOE_EP_DEVERR_EXPERT_RANGE and bits & ep.MOE_EP_DEVERR_DUPLICATE
+    with pytest.raises(ep.MoeEpError) as e:
+        p.num_recv_tokens()
+    assert e.value.status == ep.MOE_EP_ERR_DEVICE
+    p.clear_device_errors()
+    L_o, st = oracle.layout(idx, E, R, oracle.MODE_HT)
+    assert st == oracle.ERR_INVALID
+    assert np.array_equal(p.layout()["row"].cpu().numpy(), L_o["row"])
+    total, _, _ = p.num_recv_tokens()
+    assert total == T * k - 3
+    p.dispatch(torch.ones((T, H), dtype=torch.bfloat16, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.all(guard[p.rows:] == 7)
+    assert torch.all(guard[total:p.rows] == 7)
+    p.close()
+
+
+def test_host_argument_errors():
+    ep = _ep()
+    p = _pipe(synth.MODE_HT, 16, 4, 64, 256, 2, fp8=False)
+    s = torch.rand((10, 16), device=DEV)
+    bad = [dict(num_groups=3), dict(num_groups=4, topk_groups=5), dict(num_groups=64),
+           dict(weight_mode=9), dict(num_groups=8, topk_groups=1, group_topk=5)]
+    for kw in bad:
+        with pytest.raises(ep.MoeEpError) as e:
+            p.route(s, 10, **kw)
+        assert e.value.status == ep.MOE_EP_ERR_INVALID, kw
+    p.route(s, 10)
+    x = torch.zeros((10, 256), dtype=torch.bfloat16, device=DEV)
+    buf = torch.zeros(10 * 256 + 8, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ep.MoeEpError):       # misaligned x
+        ep.moe_ep_dispatch(p.handle, buf[1:].data_ptr(), False, p.recv_x, None, None, None, p.rows)
+    with pytest.raises(ep.MoeEpError):       # FP8 needs H % 128 == 0 and scales
+        ep.moe_ep_dispatch(p.handle, x, True, p.recv_x, None, None, None, p.rows)
+    with pytest.raises(ep.MoeEpError):       # too few receive rows
+        ep.moe_ep_dispatch(p.handle, x, False, p.recv_x, None, None, None, 19)
+    with pytest.raises(ep.MoeEpError):       # out overlapping y
+        ep.moe_ep_combine(p.handle, p.recv_x, p.topk_w, p.recv_x, p.rows)
+    h2 = ep.moe_ep_create_handle(p.group, 2)
+    with pytest.raises(ep.MoeEpError):       # dispatch before any route
+        ep.moe_ep_dispatch(h2, x, False, p.recv_x, None, None, None, p.rows)
+    with pytest.raises(ep.MoeEpError):       # group with live handles
+        ep.moe_ep_destroy_group(p.group)
+    ep.moe_ep_destroy_handle(h2)
+    p.close()
+
+
+def test_hot_expert_every_token():
+    """All tokens pick the same experts: one expert receives T rows."""
+    T, E, R, H, k = 1000, 32, 8, 256, 4
+    s = np.zeros((T, E), np.float32)
+    s[:, [3, 17, 30, 5]] = [4, 3, 2, 1]
+    rng = np.random.default_rng(2)
+    x = synth.tokens_bf16(rng, T, H)
+    for mode, S in ((synth.MODE_HT, T), (synth.MODE_LL, T)):
+        p = _pipe(mode, E, R, S, H, k)
+        p.route(torch.from_numpy(s).to(DEV), T, weight_mode=synth.W_SOFTMAX_TOPK)
+        p.dispatch(to_dev_bf16(x, DEV))
+        out = p.combine(p.recv_x)
+        torch.cuda.synchronize()
+        L = p.layout()
+        assert L["cnt"].cpu().numpy()[[3, 5, 17, 30]].tolist() == [T] * 4
+        assert bf16_ulp_diff(bf16_bits(out), x).max() <= 1
+        assert np.array_equal(p.topk_idx[:T].cpu().numpy()[0], [3, 17, 30, 5])
+        p.close()
+
+
+def test_two_calls_in_a_row_reuse_the_handle():
+    w = synth.WORKLOADS["ht_prefill"].with_tokens(200)
+    p = _pipe(w.mode, w.E, w.R, w.T, w.H, w.k)
+    rng = np.random.default_rng(5)
+    for T in (200, 57):
+        s = synth.uniform_bias_scores(rng, T, w.E)
+        x = synth.tokens_bf16(rng, T, w.H)
+        p.route(torch.from_numpy(s).to(DEV), T, w.G, w.kg)
+        p.num_recv_tokens()
+        p.dispatch(to_dev_bf16(x, DEV))
+        out = p.combine(p.recv_x)
+        torch.cuda.synchronize()
+        idx_o, _ = oracle.route(s, w.k, w.G, w.kg)
+        assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
+        assert bf16_ulp_diff(bf16_bits(out), x).max() <= 1
+    p.close()

@@ -1,0 +1,158 @@
+"""GPU parity: libmoeep (through the C ABI) against the CPU oracle on the same
+seeded inputs, for the five workloads.
+
+Reduced token counts (several 32-token tiles plus a ragged tail) are compared
+element by element; the full-size workloads, in the launch configuration the
+benchmark times, compare routing and layout in full and dispatch / combine on
+sampled rows and tokens the oracle computes one by one.  Tolerances: see
+tests/parity.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_layout_gb300 import synth
+from parity import W_RTOL, bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+def _pipeline(w):
+    from combine_layout_gb300.pipeline import EpPipeline
+    return EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV)
+
+
+def _check_route_layout(w, p, inp):
+    idx = p.topk_idx[: w.T].cpu().numpy()
+    wg = p.topk_w[: w.T].cpu().numpy()
+    idx_o, w_o = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+    assert np.array_equal(idx, idx_o), "topk_idx differs"
+    np.testing.assert_allclose(wg, w_o, rtol=W_RTOL, atol=0)
+    L = {k: v.cpu().numpy() for k, v in p.layout().items()}
+    L_o, st = oracle.layout(idx_o, w.E, w.R, w.mode, w.slots)
+    assert st == oracle.OK
+    for key in ("cnt", "off", "rcnt", "roff", "row"):
+        assert np.array_equal(L[key], L_o[key]), key
+    return idx_o, wg, L_o
+
+
+def _run(w, sample=None, seed=None):
+    inp = synth.make_inputs(w, seed)
+    p = _pipeline(w)
+    scores = torch.from_numpy(inp["scores"]).to(DEV)
+    x = to_dev_bf16(inp["x"], DEV)
+    p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode)
+    total, per_rank, per_expert = p.num_recv_tokens()
+    p.dispatch(x)
+    torch.cuda.synchronize()
+    idx_o, wg, L_o = _check_route_layout(w, p, inp)
+
+    if w.mode == synth.MODE_HT:
+        assert total == w.T * w.k
+        assert per_rank == L_o["rcnt"].tolist() and per_expert == L_o["cnt"].tolist()
+    else:
+        assert total == w.E * w.slots
+    assert np.array_equal(p.recv_cnt.cpu().numpy(), L_o["cnt"])
+
+    rows = defined_rows(w.mode, L_o["cnt"], w.slots, int(L_o["off"][-1]))
+    if sample is not None and rows.size > sample:
+        rng = np.random.default_rng(123)
+        rows = np.unique(np.concatenate([rows[:64], rows[-64:], rng.choice(rows, sample)]))
+    src = p.recv_src.cpu().numpy()[rows]
+    # where every pair's token lands, by the oracle's layout
+    want_src = np.empty(p.rows, np.int64)
+    flat = L_o["row"].ravel()
+    ok = flat >= 0
+    want_src[flat[ok]] = np.nonzero(ok)[0] // w.k
+    assert np.array_equal(src, want_src[rows]), "recv_src differs"
+
+    rows_t = torch.from_numpy(rows).to(DEV)
+    if w.fp8:
+        q = p.recv_x.index_select(0, rows_t).cpu().numpy()
+        sc = p.recv_scale.index_select(0, rows_t).cpu().numpy()
+        for i, t in enumerate(want_src[rows]):
+            qo, so = oracle.quant_row(inp["x"][t])
+            assert np.array_equal(q[i], qo), f"FP8 bytes differ at row {rows[i]}"
+            assert np.array_equal(sc[i], so), f"scales differ at row {rows[i]}"
+        y = dequant_on_device(p.recv_x, p.recv_scale)
+    else:
+        got = bf16_bits(p.recv_x.index_select(0, rows_t))
+        assert np.array_equal(got, inp["x"][want_src[rows]]), "bf16 payload differs"
+        y = p.recv_x
+
+    out = p.combine(y)
+    torch.cuda.synchronize()
+    tokens = np.arange(w.T)
+    if sample is not None and w.T > sample:
+        rng = np.random.default_rng(7)
+        tokens = np.unique(np.concatenate([tokens[:32], tokens[-32:], rng.choice(w.T, sample)]))
+    # the oracle sees exactly the rows these tokens read, compacted
+    r = L_o["row"][tokens]
+    flat = r.ravel()
+    valid = flat >= 0
+    gather = torch.from_numpy(np.where(valid, flat, 0).astype(np.int64)).to(DEV)
+    y_c = bf16_bits(y.index_select(0, gather))
+    row_c = np.where(valid, np.arange(flat.size), -1).reshape(r.shape).astype(np.int32)
+    want = oracle.combine(y_c, row_c, wg[tokens])
+    got = bf16_bits(out[torch.from_numpy(tokens).to(DEV)])
+    d = bf16_ulp_diff(got, want)
+    assert d.max() <= 1, f"combine differs by {d.max()} bf16 ulp"
+    # round trip: identity experts, weights summing to 1, bf16 payload -> x within 1 ulp
+    if not w.fp8:
+        rt = bf16_ulp_diff(got, inp["x"][tokens])
+        assert rt.max() <= 1, f"round trip off by {rt.max()} ulp"
+    p.close()
+    return d
+
+
+@pytest.mark.parametrize("name,T", [("tiny_ll", 128), ("tiny_ll", 77), ("ll_decode", 128),
+                                    ("ll_decode", 45), ("ht_prefill", 300), ("ht_prefill_fp8", 300),
+                                    ("mixtral", 1000), ("skewed", 333)])
+def test_parity_elementwise(name, T):
+    w = synth.WORKLOADS[name].with_tokens(T, slots=synth.WORKLOADS[name].slots or None)
+    _run(w)
+
+
+@pytest.mark.parametrize("name", ["tiny_ll", "ll_decode", "ht_prefill", "ht_prefill_fp8",
+                                  "mixtral", "skewed"])
+def test_parity_full_size(name):
+    _run(synth.WORKLOADS[name], sample=1024)
+
+
+def test_fp8_conversion_sweep_all_bf16_values():
+    """Blocks whose maximum is 448 have scale exactly 1, so the payload is the
+    plain e4m3 conversion of every finite bf16 value of magnitude <= 448."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = synth.bf16_bits_to_f32(bits)
+    vals = bits[np.isfinite(f) & (np.abs(f) <= 448)]
+    per_block = 127
+    nblk = -(-vals.size // per_block)
+    H = 7168
+    T = -(-nblk // (H // 128)) + 1          # last token: the tiny-magnitude block
+    blocks = np.zeros((T * (H // 128), 128), np.uint16)
+    blocks[:, 0] = synth.f32_to_bf16_bits(np.array([448.0], np.float32))[0]
+    flat = np.zeros(T * (H // 128) * per_block, np.uint16)
+    flat[: vals.size] = vals
+    blocks[:, 1:] = flat.reshape(-1, per_block)
+    x = blocks.reshape(T, H)
+    # tiny-magnitude blocks: subnormal bf16 inputs, scales in fp32's subnormal range
+    x[-1, :128] = np.arange(128, dtype=np.uint16)
+    from combine_layout_gb300.pipeline import EpPipeline
+    p = EpPipeline(synth.MODE_HT, 8, 2, T, H, 1, fp8=True, device=DEV)
+    idx = torch.zeros((T, 1), dtype=torch.int32, device=DEV)
+    p.route_given(idx)
+    p.dispatch(to_dev_bf16(x, DEV))
+    torch.cuda.synchronize()
+    q = p.recv_x[:T].cpu().numpy()
+    s = p.recv_scale[:T].cpu().numpy()
+    for t in range(T):
+        qo, so = oracle.quant_row(x[t])
+        assert np.array_equal(s[t], so)
+        assert np.array_equal(q[t], qo), t
+    assert np.all(s[:-1] == 1.0)
+    p.close()
