@@ -32,12 +32,15 @@ struct moe_ep_handle {
     int32_t* rcnt;        // [R]
     int32_t* roff;        // [R+1]
     int32_t* row;         // [max_tokens * max_topk]
+    int32_t* idx;         // [max_tokens * max_topk], copy of the routing
+    unsigned* done;       // layout CTA counter
     // pinned host staging for the receive-count query: off[E+1] then rcnt[R]
     int32_t* host_stage;
     // state of the last route
     int routed;
+    int rows_ready;       // row[] written for the last route
     int T, k;
-    int64_t host_total;  // total rows known on the host (-1: not queried)
+    int64_t host_total;   // total rows known on the host (-1: not queried)
 };
 
 namespace {
@@ -70,6 +73,45 @@ int64_t required_rows(const moe_ep_handle* h)
     if (g->mode == MOE_EP_LL) return (int64_t)g->E * g->S;
     if (h->host_total >= 0) return h->host_total;
     return (int64_t)h->T * h->k;
+}
+
+LayoutArgs layout_args(const moe_ep_handle* h, int T)
+{
+    LayoutArgs a;
+    a.tile_word = h->tile_word;
+    a.tile_base = h->tile_base;
+    a.cnt = h->cnt;
+    a.off = h->off;
+    a.rcnt = h->rcnt;
+    a.roff = h->roff;
+    a.done = h->done;
+    a.E = h->g->E;
+    a.R = h->g->R;
+    a.ntiles = (T + kTileTokens - 1) / kTileTokens;
+    return a;
+}
+
+RowArgs row_args(const moe_ep_handle* h)
+{
+    RowArgs a;
+    a.idx = h->idx;
+    a.tile_word = h->tile_word;
+    a.tile_base = h->tile_base;
+    a.off = h->off;
+    a.T = h->T;
+    a.k = h->k;
+    a.E = h->g->E;
+    a.S = h->g->S;
+    a.mode = h->g->mode;
+    return a;
+}
+
+int ensure_rows(moe_ep_handle* h, cudaStream_t s)
+{
+    if (h->rows_ready) return MOE_EP_OK;
+    int st = cuda_status(launch_rowmap(row_args(h), h->row, h->g->sm_count, s));
+    if (st == MOE_EP_OK) h->rows_ready = 1;
+    return st;
 }
 
 }  // namespace
@@ -155,8 +197,8 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->ntiles_max = (g->S + kTileTokens - 1) / kTileTokens;
     const size_t nt = (size_t)h->ntiles_max * g->E;
     // one allocation, carved in this order, each piece 256-byte aligned
-    const size_t counts[7] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
-                              (size_t)g->R + 1, (size_t)g->S * max_topk};
+    const size_t counts[9] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+                              (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -172,6 +214,13 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->rcnt = carve<int32_t>(cur, counts[4]);
     h->roff = carve<int32_t>(cur, counts[5]);
     h->row = carve<int32_t>(cur, counts[6]);
+    h->idx = carve<int32_t>(cur, counts[7]);
+    h->done = carve<unsigned>(cur, counts[8]);
+    if (cudaMemset(base, 0, bytes) != cudaSuccess) {
+        cudaFree(base);
+        delete h;
+        return MOE_EP_ERR_CUDA;
+    }
     void* hs = nullptr;
     if (cudaHostAlloc(&hs, sizeof(int32_t) * (size_t)(g->E + 1 + g->R), cudaHostAllocDefault) !=
         cudaSuccess) {
@@ -181,6 +230,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     }
     h->host_stage = (int32_t*)hs;
     h->routed = 0;
+    h->rows_ready = 0;
     h->host_total = -1;
     g->handles += 1;
     *out = h;
@@ -211,9 +261,16 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (T > g->S) return MOE_EP_ERR_OVERFLOW;
     if (T > 0 && !topk_idx) return MOE_EP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
-    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+    const LayoutArgs la = layout_args(h, T);
 
-    if (scores) {
+    if (T == 0) {
+        // no pairs: counts and offsets are zero
+        cudaError_t e = cudaMemsetAsync(h->cnt, 0, sizeof(int32_t) * (size_t)g->E, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->off, 0, sizeof(int32_t) * (size_t)(g->E + 1), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->rcnt, 0, sizeof(int32_t) * (size_t)g->R, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->roff, 0, sizeof(int32_t) * (size_t)(g->R + 1), s);
+        st = cuda_status(e);
+    } else if (scores) {
         RouteParams p;
         p.E = g->E;
         p.G = opts->num_groups;
@@ -236,18 +293,15 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
         }
         p.epl = (p.gs + p.lpg - 1) / p.lpg;
         if (p.epl > kMaxExpertsPerLane) return MOE_EP_ERR_INVALID;
-        st = cuda_status(launch_route(scores, T, p, topk_idx, topk_w, h->tile_word, s));
+        p.vec4 = (p.epl % 4 == 0 && p.gs == p.lpg * p.epl && g->E % 4 == 0 &&
+                  ((uintptr_t)scores & 15u) == 0) ? 1 : 0;
+        st = cuda_status(launch_route(scores, T, p, topk_idx, h->idx, topk_w, la, s));
     } else {
-        st = cuda_status(launch_layout_bits(topk_idx, T, k, g->E, h->tile_word, g->err_dev, s));
+        st = cuda_status(launch_layout_bits(topk_idx, T, k, h->idx, la, g->err_dev, s));
     }
     if (st != MOE_EP_OK) return st;
-    st = cuda_status(launch_layout_scan(h->tile_word, ntiles, g->E, h->tile_base, h->cnt, s));
-    if (st != MOE_EP_OK) return st;
-    st = cuda_status(launch_rowmap(topk_idx, T, k, g->E, g->R, g->mode, g->S, h->tile_word,
-                                   h->tile_base, h->cnt, h->off, h->rcnt, h->roff, h->row,
-                                   g->sm_count, s));
-    if (st != MOE_EP_OK) return st;
     h->routed = 1;
+    h->rows_ready = 0;
     h->T = T;
     h->k = k;
     h->host_total = -1;
@@ -307,9 +361,11 @@ int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, flo
     }
     if (recv_src && ((uintptr_t)recv_src & 3u)) return MOE_EP_ERR_INVALID;
     if (recv_cnt && ((uintptr_t)recv_cnt & 3u)) return MOE_EP_ERR_INVALID;
-    return cuda_status(launch_dispatch(x, h->T, g->H, h->k, fp8, h->row, recv_x, recv_scale,
-                                       recv_src, h->cnt, recv_cnt, g->E, g->sm_count,
-                                       (cudaStream_t)stream));
+    st = cuda_status(launch_dispatch(row_args(h), x, g->H, fp8, h->row, recv_x, recv_scale,
+                                     recv_src, h->cnt, recv_cnt, g->sm_count,
+                                     (cudaStream_t)stream));
+    if (st == MOE_EP_OK) h->rows_ready = 1;
+    return st;
 }
 
 int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
@@ -331,6 +387,8 @@ int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* 
         const char* oe = ob + (size_t)h->T * g->H * 2;
         if (ob < ye && yb < oe) return MOE_EP_ERR_INVALID;
     }
+    st = ensure_rows(h, (cudaStream_t)stream);
+    if (st != MOE_EP_OK) return st;
     return cuda_status(launch_combine(y, h->T, g->H, h->k, h->row, topk_w, out, g->sm_count,
                                       (cudaStream_t)stream));
 }
@@ -342,6 +400,10 @@ int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* r
     if (!h->routed) return MOE_EP_ERR_INVALID;
     moe_ep_group* g = h->g;
     cudaStream_t s = (cudaStream_t)stream;
+    if (row && h->T > 0) {
+        int st = ensure_rows(h, s);
+        if (st != MOE_EP_OK) return st;
+    }
     cudaError_t e = cudaSuccess;
     if (cnt && e == cudaSuccess)
         e = cudaMemcpyAsync(cnt, h->cnt, sizeof(int32_t) * g->E, cudaMemcpyDefault, s);

@@ -34,32 +34,49 @@ struct RouteParams {
     int lpg_log2;
     int epl;    // experts held per lane
     int limit;  // 1 when some groups are banned
+    int vec4;   // 1 when every lane's experts can be read as float4
 };
 
-// Router: one warp per token, one 32-token tile per CTA.  Writes topk_idx,
-// topk_w and the tile's expert bitmap words tile_word[tile][E].
+// Where the layout lives (the handle's workspace).
+struct LayoutArgs {
+    uint32_t* tile_word;  // [ntiles][E]
+    int32_t* tile_base;   // [ntiles][E]
+    int32_t* cnt;         // [E]
+    int32_t* off;         // [E+1]
+    int32_t* rcnt;        // [R]
+    int32_t* roff;        // [R+1]
+    unsigned* done;       // CTAs finished (reset to 0 by the last one)
+    int E, R, ntiles;
+};
+
+// What placing a pair into its receive row needs.
+struct RowArgs {
+    const int32_t* idx;        // handle copy of topk_idx [T][k]
+    const uint32_t* tile_word;
+    const int32_t* tile_base;
+    const int32_t* off;
+    int T, k, E, S, mode;
+};
+
+// Router: one warp per token, one 32-token tile per CTA.  Writes topk_idx
+// (caller's and the handle's copy), topk_w, the tile words, and -- in the
+// last CTA to finish -- tile_base, cnt, off, rcnt, roff.
 cudaError_t launch_route(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
-                         float* topk_w, uint32_t* tile_word, cudaStream_t s);
+                         int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s);
 
-// Bitmap words for caller-made topk_idx, with validity checks.
-cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int E, uint32_t* tile_word,
-                               volatile unsigned* err, cudaStream_t s);
+// Same layout from caller-made topk_idx, with validity checks.
+cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* idx_copy,
+                               const LayoutArgs& la, volatile unsigned* err, cudaStream_t s);
 
-// Column prefix over tiles: tile_base[tile][e] and cnt[e].
-cudaError_t launch_layout_scan(const uint32_t* tile_word, int ntiles, int E, int32_t* tile_base,
-                               int32_t* cnt, cudaStream_t s);
-
-// Offsets (off, rcnt, roff, total) and the row map row[t][j].
-cudaError_t launch_rowmap(const int32_t* topk_idx, int T, int k, int E, int R, int mode, int S,
-                          const uint32_t* tile_word, const int32_t* tile_base, const int32_t* cnt,
-                          int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row,
-                          int sm_count, cudaStream_t s);
+// Row map row[t][j] (dispatch writes it itself; this serves combine or a
+// layout copy that comes without a dispatch).
+cudaError_t launch_rowmap(const RowArgs& ra, int32_t* row, int sm_count, cudaStream_t s);
 
 // Dispatch pack: x bf16 [T][H] -> receive rows (bf16 copy or FP8 + scales).
-cudaError_t launch_dispatch(const void* x, int T, int H, int k, int fp8, const int32_t* row,
+// Also writes the row map and recv_src, and copies cnt into recv_cnt.
+cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
-                            const int32_t* cnt, int32_t* recv_cnt, int E, int sm_count,
-                            cudaStream_t s);
+                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s);
 
 // Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,

@@ -7,141 +7,151 @@
 // one scale per 128 elements.  Here the "send" to logical rank r is a store
 // into rank r's rows of the receive buffer in this GPU's memory.
 //
-// The work is HBM-bound (read H*2 bytes per token, write k rows): each CTA
-// takes one token at a time, reads it once in 16-byte vectors, converts it
-// once (FP8) and streams it to the k destination rows.
+// HBM-bound (read 2H bytes per token, write k rows).  One warp per token: the
+// k lanes compute the pair rows from the layout (and store the row map), then
+// the warp reads the token once in 16-byte vectors, converts it once (FP8) and
+// streams it to the k rows.  No block-level barrier anywhere.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include "common.cuh"
+#include "layout_dev.cuh"
 
 namespace moeep {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kUnroll = 8;  // 16-byte vectors held per thread per pass
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kThreads = 256;  // 8 warps, 8 tokens in flight per CTA
 
-__device__ __forceinline__ void load_rows(const int32_t* __restrict__ row, int t, int k,
-                                          int32_t* __restrict__ recv_src, int* s_row)
+// Rows of token t: lane j < k gets row(t, j); also stores the row map and the
+// source id of every written row.
+__device__ __forceinline__ int place_token(const RowArgs& ra, int t, int lane, int32_t* row,
+                                           int32_t* recv_src)
 {
-    if (threadIdx.x < k) {
-        const int r = row[(size_t)t * k + threadIdx.x];
-        s_row[threadIdx.x] = r;
+    const int r = token_pair_row(ra, t, lane);
+    if (lane < ra.k) {
+        row[(size_t)t * ra.k + lane] = r;
         if (r >= 0 && recv_src) recv_src[r] = t;
     }
+    return r;
 }
 
+template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
-    const uint4* __restrict__ x, int T, int k, int nvec, const int32_t* __restrict__ row,
+    RowArgs ra, const uint4* __restrict__ x, int nvec, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
-    int32_t* __restrict__ recv_cnt, int E)
+    int32_t* __restrict__ recv_cnt)
 {
-    __shared__ int s_row[kMaxTopk];
     if (blockIdx.x == 0 && recv_cnt)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) recv_cnt[e] = cnt[e];
-
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        load_rows(row, t, k, recv_src, s_row);
-        __syncthreads();
+        for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
+    const int lane = threadIdx.x & 31, wpc = blockDim.x >> 5;
+    for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < ra.T; t += gridDim.x * wpc) {
+        const int r = place_token(ra, t, lane, row, recv_src);
         const uint4* xt = x + (size_t)t * nvec;
-        for (int v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * kThreads) {
-            uint4 buf[kUnroll];
+        for (int c0 = 0; c0 < nvec; c0 += 32 * U) {
+            uint4 buf[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int v = v0 + u * kThreads;
+            for (int u = 0; u < U; ++u) {
+                const int v = c0 + u * 32 + lane;
                 if (v < nvec) buf[u] = __ldg(xt + v);
             }
-            for (int j = 0; j < k; ++j) {
-                const int r = s_row[j];
-                if (r < 0) continue;
-                uint4* dst = recv_x + (size_t)r * nvec;
+            for (int j = 0; j < ra.k; ++j) {
+                const int rj = __shfl_sync(kFull, r, j);
+                if (rj < 0) continue;
+                uint4* dst = recv_x + (size_t)rj * nvec;
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int v = v0 + u * kThreads;
+                for (int u = 0; u < U; ++u) {
+                    const int v = c0 + u * 32 + lane;
                     if (v < nvec) dst[v] = buf[u];
                 }
             }
         }
-        __syncthreads();
     }
 }
 
-// Half-warp (16 lanes x 8 elements) covers exactly one 128-element block.
+// A half-warp (16 lanes x 8 elements) covers exactly one 128-element block.
+template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
-    const uint4* __restrict__ x, int T, int k, int nvec, const int32_t* __restrict__ row,
+    RowArgs ra, const uint4* __restrict__ x, int nvec, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
-    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt, int E)
+    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
 {
-    __shared__ int s_row[kMaxTopk];
     if (blockIdx.x == 0 && recv_cnt)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) recv_cnt[e] = cnt[e];
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
+    const int lane = threadIdx.x & 31, wpc = blockDim.x >> 5;
     const int nblk = nvec / 16;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        load_rows(row, t, k, recv_src, s_row);
-        __syncthreads();
+    for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < ra.T; t += gridDim.x * wpc) {
+        const int r = place_token(ra, t, lane, row, recv_src);
         const uint4* xt = x + (size_t)t * nvec;
-        // the loop bound is uniform per warp so that every shuffle has all 32 lanes
-        for (int v0 = warp * 32; v0 < nvec; v0 += kThreads) {
-            const int v = v0 + lane;
-            const bool act = v < nvec;
-            uint4 raw = act ? __ldg(xt + v) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            float f[8];
+        for (int c0 = 0; c0 < nvec; c0 += 32 * U) {
+            uint2 q[U];
+            float sc[U];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[2 * i] = __uint_as_float(w[i] << 16);
-                f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            for (int u = 0; u < U; ++u) {
+                const int v = c0 + u * 32 + lane;
+                const uint4 raw = (v < nvec) ? __ldg(xt + v) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    f[2 * i] = __uint_as_float(w[i] << 16);
+                    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+                const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+                uint32_t packed[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                        make_float2(__fdiv_rn(f[4 * h + 0], scale), __fdiv_rn(f[4 * h + 1], scale)),
+                        __NV_SATFINITE, __NV_E4M3);
+                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                        make_float2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)),
+                        __NV_SATFINITE, __NV_E4M3);
+                    packed[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                q[u] = make_uint2(packed[0], packed[1]);
+                sc[u] = scale;
             }
-            float amax = 0.f;
+            for (int j = 0; j < ra.k; ++j) {
+                const int rj = __shfl_sync(kFull, r, j);
+                if (rj < 0) continue;
+                uint2* dst = recv_q + (size_t)rj * nvec;
+                float* sdst = recv_scale + (size_t)rj * nblk;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
-            uint32_t packed[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(f[4 * h + 0], scale), __fdiv_rn(f[4 * h + 1], scale)),
-                    __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)),
-                    __NV_SATFINITE, __NV_E4M3);
-                packed[h] = (uint32_t)lo | ((uint32_t)hi << 16);
-            }
-            if (act) {
-                const uint2 q = make_uint2(packed[0], packed[1]);
-                for (int j = 0; j < k; ++j) {
-                    const int r = s_row[j];
-                    if (r < 0) continue;
-                    recv_q[(size_t)r * nvec + v] = q;
-                    if ((lane & 15) == 0) recv_scale[(size_t)r * nblk + v / 16] = scale;
+                for (int u = 0; u < U; ++u) {
+                    const int v = c0 + u * 32 + lane;
+                    if (v < nvec) {
+                        dst[v] = q[u];
+                        if ((lane & 15) == 0) sdst[v >> 4] = sc[u];
+                    }
                 }
             }
         }
-        __syncthreads();
     }
 }
 
 }  // namespace
 
-cudaError_t launch_dispatch(const void* x, int T, int H, int k, int fp8, const int32_t* row,
+cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
-                            const int32_t* cnt, int32_t* recv_cnt, int E, int sm_count,
-                            cudaStream_t s)
+                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s)
 {
     const int nvec = H / 8;
-    int blocks = T < 1 ? 1 : T;
-    const int cap = sm_count * 16;
-    if (blocks > cap) blocks = cap;
+    const int wpc = kThreads / 32;
+    int blocks = (ra.T + wpc - 1) / wpc;
+    if (blocks < 1) blocks = 1;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
     if (fp8)
-        dispatch_fp8_kernel<<<blocks, kThreads, 0, s>>>(
-            (const uint4*)x, T, k, nvec, row, (uint2*)recv_x, recv_scale, recv_src, cnt, recv_cnt, E);
+        dispatch_fp8_kernel<4><<<blocks, kThreads, 0, s>>>(ra, (const uint4*)x, nvec, row,
+                                                           (uint2*)recv_x, recv_scale, recv_src,
+                                                           cnt, recv_cnt);
     else
-        dispatch_bf16_kernel<<<blocks, kThreads, 0, s>>>((const uint4*)x, T, k, nvec, row,
-                                                         (uint4*)recv_x, recv_src, cnt, recv_cnt, E);
+        dispatch_bf16_kernel<7><<<blocks, kThreads, 0, s>>>(ra, (const uint4*)x, nvec, row,
+                                                            (uint4*)recv_x, recv_src, cnt, recv_cnt);
     return cudaGetLastError();
 }
 

@@ -3,72 +3,100 @@
 // Routing follows "NVSHMEM 与 DeepEP：GPU 发起的通信", section "高吞吐模式": each node
 // (a contiguous group of E/G experts) is scored by the sum of its m best expert
 // scores, the best kg nodes are kept, and the k best experts among them are
-// chosen.  Ties: the larger score wins; on equal scores the lower index wins
-// (nodes and experts alike).  Group sums are formed in binary64 (the sum of
-// two fp32 scores is exact there), so node decisions do not depend on fp32
-// rounding of the sum.  NaN scores rank as -infinity.
+// chosen, best first.  Ties: the larger score wins; on equal scores the lower
+// index wins (nodes and experts alike).  Group sums are formed in binary64 (the
+// sum of two fp32 scores is exact there) and compared exactly as ordered
+// 64-bit integers.  NaN scores rank as -infinity; -0 equals +0.
 //
 // Work split: one warp per token, one CTA per 32-token tile.  Lane l holds up
 // to `epl` consecutive experts of group l / lpg, so a group's experts live in
-// lpg adjacent lanes and its top-m merges in log2(lpg) butterfly steps.
+// lpg adjacent lanes and its top-m merges in log2(lpg) butterfly steps.  Each
+// of the k picks is two warp reductions (redux.sync): the largest score key,
+// then the lowest expert index holding it.  Scores are compared as
+// order-preserving 32-bit keys (0 is below every score: "no candidate").
 #include <limits.h>
 #include <math.h>
 
-#include "common.cuh"
+#include "layout_dev.cuh"
 
 namespace moeep {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+__device__ __forceinline__ uint32_t score_key(float x)
+{
+    if (isnan(x)) x = -INFINITY;
+    if (x == 0.f) x = 0.f;  // -0 -> +0
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_score(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ uint64_t sum_key(double d)
+{
+    if (isnan(d)) d = -INFINITY;
+    const uint64_t u = (uint64_t)__double_as_longlong(d);
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
 template <int M>
-__device__ __forceinline__ void insert_desc(float (&t)[M], float x)
+__device__ __forceinline__ void insert_desc(uint32_t (&t)[M], uint32_t x)
 {
 #pragma unroll
     for (int q = 0; q < M; ++q) {
-        if (x > t[q]) {
-            float o = t[q];
-            t[q] = x;
-            x = o;
-        }
+        const uint32_t hi = max(t[q], x), lo = min(t[q], x);
+        t[q] = hi;
+        x = lo;
     }
 }
 
-// (value, index) ordering: larger value first, lower index on ties.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi)
-{
-    return v > bv || (v == bv && i < bi);
-}
-
-template <int EPL>
+template <int EPL, bool VEC>
 __device__ __forceinline__ void route_token(const float* __restrict__ s, const RouteParams& p,
                                             int lane, int& out_idx, float& out_w)
 {
     const int grp = lane >> p.lpg_log2;
     const int sub = lane & (p.lpg - 1);
-    const int first = sub * p.epl;           // offset of my first expert inside the group
-    const int base = grp * p.gs + first;     // global id of my first expert
+    const int first = sub * p.epl;        // offset of my first expert inside the group
+    const int base = grp * p.gs + first;  // global id of my first expert
 
-    float v[EPL];
+    uint32_t key[EPL];
     uint32_t inr = 0;
+    if (VEC) {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const bool in = (grp < p.G) && (i < p.epl) && (first + i < p.gs);
-        const float x = in ? __ldg(s + base + i) : -INFINITY;
-        v[i] = isnan(x) ? -INFINITY : x;  // a NaN score ranks below every number
-        if (in) inr |= 1u << i;
+        for (int i4 = 0; i4 < EPL / 4; ++i4) {
+            const bool in = (grp < p.G) && (4 * i4 < p.epl);
+            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (in) f = __ldg(reinterpret_cast<const float4*>(s + base) + i4);
+            key[4 * i4 + 0] = score_key(f.x);
+            key[4 * i4 + 1] = score_key(f.y);
+            key[4 * i4 + 2] = score_key(f.z);
+            key[4 * i4 + 3] = score_key(f.w);
+            if (in) inr |= 0xfu << (4 * i4);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const bool in = (grp < p.G) && (i < p.epl) && (first + i < p.gs);
+            key[i] = in ? score_key(__ldg(s + base + i)) : 0u;
+            if (in) inr |= 1u << i;
+        }
     }
 
-    uint32_t ok = inr;
+    uint32_t rem = inr;
     if (p.limit) {
-        float top[kMaxGroupTopk];
+        uint32_t top[kMaxGroupTopk];
 #pragma unroll
-        for (int q = 0; q < kMaxGroupTopk; ++q) top[q] = -INFINITY;
+        for (int q = 0; q < kMaxGroupTopk; ++q) top[q] = 0u;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if ((inr >> i) & 1u) insert_desc(top, v[i]);
+            if ((inr >> i) & 1u) insert_desc(top, key[i]);
         for (int o = 1; o < p.lpg; o <<= 1) {
-            float oth[kMaxGroupTopk];
+            uint32_t oth[kMaxGroupTopk];
 #pragma unroll
             for (int q = 0; q < kMaxGroupTopk; ++q) oth[q] = __shfl_xor_sync(kFull, top[q], o);
 #pragma unroll
@@ -78,67 +106,62 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         double gsum = 0.0;
 #pragma unroll
         for (int q = kMaxGroupTopk - 1; q >= 0; --q)
-            if (q < p.m) gsum += (double)top[q];
+            if (q < p.m) gsum += (double)key_score(top[q]);
+        const unsigned long long gk = sum_key(gsum);
         int rank = 0;
         for (int n = 0; n < p.G; ++n) {
-            const double o = __shfl_sync(kFull, gsum, n << p.lpg_log2);
-            if (o > gsum || (o == gsum && n < grp)) ++rank;
+            const unsigned long long o = __shfl_sync(kFull, gk, n << p.lpg_log2);
+            rank += (o > gk || (o == gk && n < grp)) ? 1 : 0;
         }
-        if (rank >= p.kg) ok = 0;
+        if (grp >= p.G || rank >= p.kg) rem = 0u;
     }
 
-    // k rounds of warp arg-max; lane j keeps the j-th pick
-    int my_i = 0;
-    float my_v = 0.f;
+    // k picks: largest key, then lowest index holding it
+    int my_i = -1;
+    uint32_t my_k = 0u, first_k = 0u;
+    float den = 0.f;
     for (int j = 0; j < p.k; ++j) {
-        float bv = -INFINITY;
+        uint32_t bk = 0u;
         int bi = INT_MAX;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if (((ok >> i) & 1u) && better(v[i], base + i, bv, bi)) {
-                bv = v[i];
+            if (((rem >> i) & 1u) && key[i] > bk) {
+                bk = key[i];
                 bi = base + i;
             }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(kFull, bv, o);
-            const int oi = __shfl_xor_sync(kFull, bi, o);
-            if (better(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        const int iw = bi - base;
-        if (iw >= 0 && iw < EPL && ((ok >> iw) & 1u)) ok &= ~(1u << iw);
+        const uint32_t mk = __reduce_max_sync(kFull, bk);
+        const uint32_t wi = __reduce_min_sync(kFull, (bk == mk) ? (uint32_t)bi : 0xffffffffu);
+        const bool found = mk != 0u;
+        if (found && bk == mk && (uint32_t)bi == wi) rem &= ~(1u << (bi - base));
         if (lane == j) {
-            my_i = (bi == INT_MAX) ? -1 : bi;  // unreachable while kg * gs >= k
-            my_v = bv;
+            my_i = found ? (int)wi : -1;  // not found is unreachable while kg * gs >= k
+            my_k = mk;
         }
+        if (j == 0) first_k = mk;
+        den += key_score(mk);
     }
 
     const bool act = lane < p.k;
+    const float my_v = key_score(my_k);
     float w;
     if (p.wmode == MOE_EP_W_SCORE_NORM) {
-        float den = 0.f;
-        for (int j = 0; j < p.k; ++j) den += __shfl_sync(kFull, my_v, j);
         w = __fdiv_rn(my_v, den);
     } else if (p.wmode == MOE_EP_W_SOFTMAX_TOPK) {
-        const float mx = __shfl_sync(kFull, my_v, 0);
+        const float mx = key_score(first_k);
         const float ex = act ? expf(my_v - mx) : 0.f;
-        float den = 0.f;
-        for (int j = 0; j < p.k; ++j) den += __shfl_sync(kFull, ex, j);
-        w = __fdiv_rn(ex, den);
+        float d = 0.f;
+        for (int j = 0; j < p.k; ++j) d += __shfl_sync(kFull, ex, j);
+        w = __fdiv_rn(ex, d);
     } else {
-        float mx = -INFINITY;
+        uint32_t mloc = 0u;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if ((inr >> i) & 1u) mx = fmaxf(mx, v[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+            if ((inr >> i) & 1u) mloc = max(mloc, key[i]);
+        const float mx = key_score(__reduce_max_sync(kFull, mloc));
         float z = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if ((inr >> i) & 1u) z += expf(v[i] - mx);
+            if ((inr >> i) & 1u) z += expf(key_score(key[i]) - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
         const float pj = act ? __fdiv_rn(expf(my_v - mx), z) : 0.f;
@@ -150,13 +173,14 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
     out_w = w;
 }
 
-template <int EPL>
-__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ scores, int T,
+template <int EPL, bool VEC>
+__global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict__ scores, int T,
                                                      RouteParams p, int32_t* __restrict__ topk_idx,
-                                                     float* __restrict__ topk_w,
-                                                     uint32_t* __restrict__ tile_word)
+                                                     int32_t* __restrict__ idx_copy,
+                                                     float* __restrict__ topk_w, LayoutArgs la)
 {
-    extern __shared__ uint32_t s_word[];  // [E]
+    __shared__ uint32_t s_word[kMaxExperts];
+    __shared__ int s_scratch[1024 + 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < p.E; e += blockDim.x) s_word[e] = 0u;
     __syncthreads();
@@ -166,24 +190,28 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ s
     if (t < T) {
         int e;
         float w;
-        route_token<EPL>(scores + (size_t)t * p.E, p, lane, e, w);
+        route_token<EPL, VEC>(scores + (size_t)t * p.E, p, lane, e, w);
         if (lane < p.k) {
-            topk_idx[(size_t)t * p.k + lane] = e;
-            if (topk_w) topk_w[(size_t)t * p.k + lane] = w;
+            const size_t q = (size_t)t * p.k + lane;
+            topk_idx[q] = e;
+            idx_copy[q] = e;
+            if (topk_w) topk_w[q] = w;
             if (e >= 0) atomicOr(&s_word[e], 1u << warp);
         }
     }
     __syncthreads();
-    for (int e = tid; e < p.E; e += blockDim.x) tile_word[(size_t)tile * p.E + e] = s_word[e];
+    for (int e = tid; e < p.E; e += blockDim.x) la.tile_word[(size_t)tile * p.E + e] = s_word[e];
+    finish_layout_if_last(la, s_scratch);
 }
 
 __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restrict__ topk_idx,
-                                                          int T, int k, int E,
-                                                          uint32_t* __restrict__ tile_word,
-                                                          volatile unsigned* err)
+                                                          int T, int k,
+                                                          int32_t* __restrict__ idx_copy,
+                                                          LayoutArgs la, volatile unsigned* err)
 {
-    extern __shared__ uint32_t s_word[];  // [E]
-    const int tid = threadIdx.x;
+    __shared__ uint32_t s_word[kMaxExperts];
+    __shared__ int s_scratch[256 + 32];
+    const int tid = threadIdx.x, E = la.E;
     for (int e = tid; e < E; e += blockDim.x) s_word[e] = 0u;
     __syncthreads();
     const int tile = blockIdx.x;
@@ -193,6 +221,7 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
         const int tl = q / k, j = q - tl * k;
         const int32_t* r = topk_idx + (size_t)(t0 + tl) * k;
         const int e = r[j];
+        idx_copy[(size_t)(t0 + tl) * k + j] = e;
         if (e == -1) continue;
         if (e < -1 || e >= E) {
             err[kErrRange] = 1u;
@@ -207,37 +236,48 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
         atomicOr(&s_word[e], 1u << tl);
     }
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) tile_word[(size_t)tile * E + e] = s_word[e];
+    for (int e = tid; e < E; e += blockDim.x) la.tile_word[(size_t)tile * E + e] = s_word[e];
+    finish_layout_if_last(la, s_scratch);
+}
+
+template <int EPL>
+void launch_route_epl(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
+                      int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
+{
+    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+    if (EPL >= 4 && p.vec4)
+        route_kernel<EPL, (EPL >= 4)><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy,
+                                                              topk_w, la);
+    else
+        route_kernel<EPL, false><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w,
+                                                         la);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
-                         float* topk_w, uint32_t* tile_word, cudaStream_t s)
+                         int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     if (T <= 0) return cudaSuccess;
-    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
-    const size_t smem = sizeof(uint32_t) * (size_t)p.E;
     if (p.epl <= 1)
-        route_kernel<1><<<ntiles, 1024, smem, s>>>(scores, T, p, topk_idx, topk_w, tile_word);
+        launch_route_epl<1>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     else if (p.epl <= 2)
-        route_kernel<2><<<ntiles, 1024, smem, s>>>(scores, T, p, topk_idx, topk_w, tile_word);
+        launch_route_epl<2>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     else if (p.epl <= 4)
-        route_kernel<4><<<ntiles, 1024, smem, s>>>(scores, T, p, topk_idx, topk_w, tile_word);
+        launch_route_epl<4>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     else if (p.epl <= 8)
-        route_kernel<8><<<ntiles, 1024, smem, s>>>(scores, T, p, topk_idx, topk_w, tile_word);
+        launch_route_epl<8>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     else
-        route_kernel<16><<<ntiles, 1024, smem, s>>>(scores, T, p, topk_idx, topk_w, tile_word);
+        launch_route_epl<16>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int E, uint32_t* tile_word,
-                               volatile unsigned* err, cudaStream_t s)
+cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* idx_copy,
+                               const LayoutArgs& la, volatile unsigned* err, cudaStream_t s)
 {
     if (T <= 0) return cudaSuccess;
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
-    layout_bits_kernel<<<ntiles, 256, sizeof(uint32_t) * (size_t)E, s>>>(topk_idx, T, k, E,
-                                                                          tile_word, err);
+    layout_bits_kernel<<<ntiles, 256, 0, s>>>(topk_idx, T, k, idx_copy, la, err);
     return cudaGetLastError();
 }
 

@@ -189,7 +189,7 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
                 qsort(tmp, (size_t)gs, sizeof(double), double_asc);
                 double sum = 0.0;
                 for (int i = gs - m; i < gs; ++i) sum += tmp[i];   /* ascending order */
-                nodes[n].v = sum;
+                nodes[n].v = isnan(sum) ? -INFINITY : sum;         /* inf + -inf ranks lowest */
                 nodes[n].i = n;
             }
             qsort(nodes, (size_t)G, sizeof(scored), by_value_asc_index_desc);
