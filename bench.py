@@ -143,7 +143,7 @@ def run_gpu(args) -> dict | None:
     import torch.distributed as dist
 
     from combine_layout_gb300 import moe_ep as ep
-    from combine_layout_gb300.pipeline import EpPipeline
+    from combine_layout_gb300.pipeline import BoundStep, EpPipeline
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -174,18 +174,20 @@ def run_gpu(args) -> dict | None:
     # last: the receive buffers hold the worst case (T*k rows), so neither the
     # dispatch nor the combine launch waits for the count, and the sync overlaps
     # the step's GPU work instead of splitting it.
+    bs = BoundStep(p, scores, x, y, w.T, w.G, w.kg, 0, w.weight_mode, stream)
+
     def step(ev=None):
-        p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode)
+        bs.route()
         if ev is not None:
             ev[0].record(stream)
-        p.dispatch(x)
+        bs.dispatch()
         if ev is not None:
             ev[1].record(stream)
-        p.combine(y)
+        bs.combine()
         if ev is not None:
             ev[2].record(stream)
         if ht:
-            p.num_recv_tokens()
+            bs.num_recv_tokens()
 
     def barrier():
         if world > 1:

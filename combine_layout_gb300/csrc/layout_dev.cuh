@@ -36,32 +36,49 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
 
     const int nthr = blockDim.x, tid = threadIdx.x;
     const int E = a.E, ntiles = a.ntiles;
-    // tpc threads share one expert column, each scanning a contiguous run of tiles
+    // tpc threads share one expert column, each scanning a contiguous run of
+    // tiles; consecutive threads take consecutive columns (coalesced loads),
+    // and each thread keeps kBatch independent loads in flight.
+    constexpr int kBatch = 16;
     int tpc = 1;
     while (tpc * 2 * E <= nthr) tpc *= 2;
     const int cols_per_pass = nthr / tpc;
-    const int col_in = tid / tpc, part = tid % tpc;
+    const int col_in = tid % cols_per_pass, part = tid / cols_per_pass;
     const int rp = (ntiles + tpc - 1) / tpc;
     const int r0 = min(part * rp, ntiles), r1 = min(r0 + rp, ntiles);
     for (int c0 = 0; c0 < E; c0 += cols_per_pass) {
         const int col = c0 + col_in;
-        const bool act = col < E && col_in < cols_per_pass;
+        const bool act = col < E && part < tpc;
         int sum = 0;
         if (act)
-            for (int r = r0; r < r1; ++r) sum += __popc(__ldcg(a.tile_word + (size_t)r * E + col));
+            for (int rb = r0; rb < r1; rb += kBatch) {
+                uint32_t w[kBatch];
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q)
+                    w[q] = (rb + q < r1) ? __ldcg(a.tile_word + (size_t)(rb + q) * E + col) : 0u;
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q) sum += __popc(w[q]);
+            }
         s_scratch[tid] = sum;
         __syncthreads();
         if (act) {
             int base = 0, total = 0;
             for (int q = 0; q < tpc; ++q) {
-                const int v = s_scratch[col_in * tpc + q];
+                const int v = s_scratch[q * cols_per_pass + col_in];
                 if (q < part) base += v;
                 total += v;
             }
             int run = base;
-            for (int r = r0; r < r1; ++r) {
-                a.tile_base[(size_t)r * E + col] = run;
-                run += __popc(__ldcg(a.tile_word + (size_t)r * E + col));
+            for (int rb = r0; rb < r1; rb += kBatch) {
+                uint32_t w[kBatch];
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q)
+                    w[q] = (rb + q < r1) ? __ldcg(a.tile_word + (size_t)(rb + q) * E + col) : 0u;
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q) {
+                    if (rb + q < r1) a.tile_base[(size_t)(rb + q) * E + col] = run;
+                    run += __popc(w[q]);
+                }
             }
             if (part == 0) a.cnt[col] = total;
         }

@@ -4,9 +4,12 @@
 // (a contiguous group of E/G experts) is scored by the sum of its m best expert
 // scores, the best kg nodes are kept, and the k best experts among them are
 // chosen, best first.  Ties: the larger score wins; on equal scores the lower
-// index wins (nodes and experts alike).  Group sums are formed in binary64 (the
-// sum of two fp32 scores is exact there) and compared exactly as ordered
-// 64-bit integers.  NaN scores rank as -infinity; -0 equals +0.
+// index wins (nodes and experts alike).  Nodes are ranked by the exact sum of
+// their m best scores: for m <= 2 an fp32 two-sum holds it exactly as a
+// (hi, lo) pair, compared as one ordered 64-bit key (binary64 for larger m).
+// NaN scores and NaN sums (inf + -inf) rank as -infinity; -0 equals +0.
+// Scores are expected below 2^126 in magnitude, so a two-score sum cannot
+// overflow fp32.
 //
 // Work split: one warp per token, one CTA per 32-token tile.  Lane l holds up
 // to `epl` consecutive experts of group l / lpg, so a group's experts live in
@@ -102,12 +105,27 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
 #pragma unroll
             for (int q = 0; q < kMaxGroupTopk; ++q) insert_desc(top, oth[q]);
         }
-        // the group's m best, summed in ascending order in binary64
-        double gsum = 0.0;
+        // Group score: the exact sum of the group's m best scores.  For m <= 2
+        // an fp32 two-sum gives it exactly as (hi, lo), and (hi, lo) pairs
+        // order like the exact sums; larger m sums in binary64, ascending.
+        unsigned long long gk;
+        if (p.m <= 2) {
+            const float a = key_score(top[0]);
+            const float b = (p.m == 2) ? key_score(top[1]) : 0.f;
+            const float hi = __fadd_rn(b, a);
+            float lo = 0.f;
+            if (isfinite(hi)) {
+                const float bb = __fsub_rn(hi, a);
+                lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+            }
+            gk = ((unsigned long long)score_key(hi) << 32) | score_key(lo);
+        } else {
+            double gsum = 0.0;
 #pragma unroll
-        for (int q = kMaxGroupTopk - 1; q >= 0; --q)
-            if (q < p.m) gsum += (double)key_score(top[q]);
-        const unsigned long long gk = sum_key(gsum);
+            for (int q = kMaxGroupTopk - 1; q >= 0; --q)
+                if (q < p.m) gsum += (double)key_score(top[q]);
+            gk = sum_key(gsum);
+        }
         int rank = 0;
         for (int n = 0; n < p.G; ++n) {
             const unsigned long long o = __shfl_sync(kFull, gk, n << p.lpg_log2);

@@ -92,3 +92,61 @@ class EpPipeline:
             self.close()
         except Exception:
             pass
+
+
+class BoundStep:
+    """One forward on fixed buffers with every C-ABI argument marshalled once.
+
+    For callers that repeat the same shapes (a serving loop, the benchmark):
+    each call is then a bare ctypes call into libmoeep, so the host adds as
+    little as possible between the kernels of a step.
+    """
+
+    def __init__(self, p: EpPipeline, scores, x, y, num_tokens: int, num_groups: int = 1,
+                 topk_groups: int = 1, group_topk: int = 0,
+                 weight_mode: int = ep.MOE_EP_W_SCORE_NORM, stream=None):
+        import ctypes
+
+        V = ctypes.c_void_p
+        if stream is None:
+            stream = torch.cuda.current_stream(p.device)
+        lib = ep._lib
+        h = V(p.handle)
+        s = V(stream.cuda_stream)
+        ptr = (lambda t: None if t is None else V(t.data_ptr()))
+        for t in (scores, x, y):
+            if not t.is_contiguous():
+                raise ValueError("libmoeep takes contiguous tensors")
+        self.p = p
+        self._opts = ep.RouteOpts(p.k, num_groups, topk_groups, group_topk, weight_mode)
+        self._total = ctypes.c_int64()
+        self._per_rank = (ctypes.c_int32 * p.R)()
+        self._route = (lib.moe_ep_route, (h, ptr(scores), num_tokens, ctypes.byref(self._opts),
+                                          ptr(p.topk_idx), ptr(p.topk_w), s))
+        self._dispatch = (lib.moe_ep_dispatch, (h, ptr(x), int(p.fp8), ptr(p.recv_x),
+                                                ptr(p.recv_scale), ptr(p.recv_src),
+                                                ptr(p.recv_cnt), p.rows, s))
+        self._combine = (lib.moe_ep_combine, (h, ptr(y), ptr(p.topk_w), ptr(p.out), y.shape[0], s))
+        self._query = (lib.moe_ep_get_num_recv_tokens,
+                       (h, ctypes.byref(self._total),
+                        ctypes.cast(self._per_rank, ctypes.c_void_p), None, s))
+        p.T = num_tokens
+
+    @staticmethod
+    def _call(fa, name):
+        st = fa[0](*fa[1])
+        if st != ep.MOE_EP_OK:
+            raise ep.MoeEpError(name, st)
+
+    def route(self):
+        self._call(self._route, "moe_ep_route")
+
+    def dispatch(self):
+        self._call(self._dispatch, "moe_ep_dispatch")
+
+    def combine(self):
+        self._call(self._combine, "moe_ep_combine")
+
+    def num_recv_tokens(self) -> int:
+        self._call(self._query, "moe_ep_get_num_recv_tokens")
+        return self._total.value

@@ -128,7 +128,8 @@ int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale)
 /* routing                                                                    */
 /* ------------------------------------------------------------------------- */
 
-typedef struct { double v; int i; } scored;
+/* v + lo is the exact value (lo = 0 unless a node score needs it) */
+typedef struct { double v; double lo; int i; } scored;
 
 /* (value descending, index ascending) */
 static int by_value_desc(const void* pa, const void* pb)
@@ -140,13 +141,16 @@ static int by_value_desc(const void* pa, const void* pb)
     return (a->i > b->i) - (a->i < b->i);
 }
 
-/* (value ascending, index descending): the first entries are the ones to ban */
+/* (exact value ascending, index descending): the first entries are the ones
+ * to ban.  (v, lo) pairs with lo the rounding error of v order like v + lo. */
 static int by_value_asc_index_desc(const void* pa, const void* pb)
 {
     const scored* a = (const scored*)pa;
     const scored* b = (const scored*)pb;
     if (a->v < b->v) return -1;
     if (a->v > b->v) return 1;
+    if (a->lo < b->lo) return -1;
+    if (a->lo > b->lo) return 1;
     return (a->i < b->i) - (a->i > b->i);
 }
 
@@ -187,9 +191,22 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
             for (int n = 0; n < G; ++n) {
                 for (int i = 0; i < gs; ++i) tmp[i] = (double)s[n * gs + i];
                 qsort(tmp, (size_t)gs, sizeof(double), double_asc);
-                double sum = 0.0;
-                for (int i = gs - m; i < gs; ++i) sum += tmp[i];   /* ascending order */
-                nodes[n].v = isnan(sum) ? -INFINITY : sum;         /* inf + -inf ranks lowest */
+                /* node score: the exact sum of the node's m best scores */
+                double sum = 0.0, lo = 0.0;
+                if (m <= 2) {
+                    /* two fp32 values: hi + lo = exact sum (Knuth's two-sum) */
+                    double a = tmp[gs - 1], b = (m == 2) ? tmp[gs - 2] : 0.0;
+                    sum = b + a;
+                    if (isfinite(sum)) {
+                        double bb = sum - a;
+                        lo = (a - (sum - bb)) + (b - bb);
+                    }
+                } else {
+                    for (int i = gs - m; i < gs; ++i) sum += tmp[i];   /* ascending order */
+                }
+                if (isnan(sum)) { sum = -INFINITY; lo = 0.0; }      /* inf + -inf ranks lowest */
+                nodes[n].v = sum;
+                nodes[n].lo = (lo == 0.0) ? 0.0 : lo;
                 nodes[n].i = n;
             }
             qsort(nodes, (size_t)G, sizeof(scored), by_value_asc_index_desc);
@@ -202,7 +219,7 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
         /* Step 2: the k best allowed experts, best first. */
         int nc = 0;
         for (int e = 0; e < E; ++e)
-            if (allowed[e]) { cand[nc].v = (double)s[e]; cand[nc].i = e; ++nc; }
+            if (allowed[e]) { cand[nc].v = (double)s[e]; cand[nc].lo = 0.0; cand[nc].i = e; ++nc; }
         qsort(cand, (size_t)nc, sizeof(scored), by_value_desc);
         for (int j = 0; j < k; ++j) topk_idx[t * k + j] = cand[j].i;
 

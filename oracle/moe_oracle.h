@@ -50,9 +50,10 @@ int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale);
 
 /* Node-limited (grouped) top-k routing, then gate weights in binary64.
  * scores [T][E] fp32; E experts in G contiguous groups (nodes) of E/G.
- * If 1 < G and kg < G: group score = sum of the group's m largest scores
- * (summed in ascending order, binary64); the G - kg groups with the lowest
- * group score are banned (on equal score the higher index is banned first).
+ * If 1 < G and kg < G: group score = the exact sum of the group's m largest
+ * scores (m <= 2: exact, as a binary64 two-sum; m > 2: summed in ascending
+ * order in binary64); the G - kg groups with the lowest group score are banned
+ * (on equal score the higher index is banned first).
  * The k best allowed experts are taken by (score desc, index asc).
  * A NaN score ranks as -infinity.
  * weight_mode: ORC_W_SOFTMAX_TOPK   softmax over the k selected scores,

@@ -207,3 +207,29 @@ def test_two_calls_in_a_row_reuse_the_handle():
         assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
         assert bf16_ulp_diff(bf16_bits(out), x).max() <= 1
     p.close()
+
+
+@pytest.mark.parametrize("E,G,kg,k,m", [(256, 8, 4, 8, 2), (64, 8, 3, 6, 2), (16, 1, 1, 2, 1),
+                                        (32, 4, 2, 4, 1), (128, 8, 2, 8, 3), (8, 1, 1, 2, 1)])
+def test_router_adversarial_scores(E, G, kg, k, m):
+    """Exact ties, wide exponent spreads (sums binary64 cannot hold), NaN, +-0
+    and +-inf: the kernel's picks equal the oracle's."""
+    rng = np.random.default_rng(E + G + k)
+    T = 333
+    s = (rng.random((T, E)) * 2.0 ** rng.integers(-80, 3, (T, E))).astype(np.float32)
+    s[::7] = np.round(s[::7] * 4) / 4                     # many exact ties
+    s[1::11, : E // 2] = 1.0                              # tied groups
+    s[2::13, 0] = np.nan
+    s[3::17, 1] = -0.0
+    s[4::19, 2] = np.inf
+    s[5::23, 3] = -np.inf
+    s[6::29] *= -1.0                                      # negative scores
+    from combine_layout_gb300.pipeline import EpPipeline
+    p = EpPipeline(synth.MODE_HT, E, E // 8 if E >= 8 else 1, T, 128, k, device=DEV)
+    p.route(torch.from_numpy(s).to(DEV), T, G, kg, m, synth.W_SCORE_NORM)
+    torch.cuda.synchronize()
+    idx_o, _ = oracle.route(s, k, G, kg, group_topk=m, weight_mode=oracle.W_SCORE_NORM)
+    got = p.topk_idx[:T].cpu().numpy()
+    bad = np.nonzero((got != idx_o).any(1))[0]
+    assert bad.size == 0, (bad[:5], got[bad[:2]], idx_o[bad[:2]])
+    p.close()

@@ -147,3 +147,31 @@ def test_no_limit_nodes_formula_matches_when_groups_all_kept(orc):
     b, wb = orc.route(s, 4)
     assert np.array_equal(a, b) and np.array_equal(wa, wb)
     assert math.isclose(float(wa.sum()), 200.0, rel_tol=1e-12)
+
+
+def test_node_scores_compare_exact_sums(orc):
+    """Node scores are exact sums: (1 + 2^-60) beats (1 + 2^-61) although both
+    round to 1.0 in binary64; exact rational arithmetic (fractions) decides."""
+    from fractions import Fraction
+    s = np.zeros((1, 8), np.float32)
+    s[0, 0:2] = [1.0, 2.0 ** -61]     # node 0
+    s[0, 2:4] = [0.5, 0.25]           # node 1: 0.75
+    s[0, 4:6] = [1.0, 2.0 ** -60]     # node 2
+    s[0, 6:8] = [0.25, 0.25]          # node 3: 0.5
+    exact = [Fraction(float(s[0, 2 * n])) + Fraction(float(s[0, 2 * n + 1])) for n in range(4)]
+    assert float(exact[0]) == float(exact[2]) and exact[2] > exact[0]
+    idx, _ = orc.route(s, 1, num_groups=4, topk_groups=1, group_topk=2)
+    assert idx[0].tolist() == [4]                       # node 2's best expert
+    idx, _ = orc.route(s, 2, num_groups=4, topk_groups=2, group_topk=2)
+    assert sorted(idx[0].tolist()) == [0, 4]            # nodes 2 and 0 (exact order)
+    # brute force with exact rationals on random tiny scores with wide exponents
+    rng = np.random.default_rng(8)
+    for trial in range(200):
+        v = (rng.random(12) * 2.0 ** rng.integers(-70, 2, 12)).astype(np.float32)
+        idx, _ = orc.route(v[None, :], 2, num_groups=6, topk_groups=2, group_topk=2)
+        gs = [sum(sorted((Fraction(float(a)) for a in v[2 * n:2 * n + 2]), reverse=True)[:2])
+              for n in range(6)]
+        kept = sorted(range(6), key=lambda n: (-gs[n], n))[:2]
+        allowed = [e for e in range(12) if e // 2 in kept]
+        want = sorted(allowed, key=lambda e: (-Fraction(float(v[e])), e))[:2]
+        assert idx[0].tolist() == want, (trial, v)
