@@ -26,6 +26,8 @@ struct moe_ep_handle {
     int ntiles_max;
     // device workspace
     uint32_t* tile_word;  // [ntiles_max][E]
+    uint8_t* tile_cnt;    // [E][cnt_stride]
+    int cnt_stride;       // ntiles_max rounded up to 16
     int32_t* tile_base;   // [ntiles_max][E]
     int32_t* cnt;         // [E]
     int32_t* off;         // [E+1]
@@ -79,6 +81,7 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
 {
     LayoutArgs a;
     a.tile_word = h->tile_word;
+    a.tile_cnt = h->tile_cnt;
     a.tile_base = h->tile_base;
     a.cnt = h->cnt;
     a.off = h->off;
@@ -88,6 +91,7 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
     a.E = h->g->E;
     a.R = h->g->R;
     a.ntiles = (T + kTileTokens - 1) / kTileTokens;
+    a.cnt_stride = h->cnt_stride;
     return a;
 }
 
@@ -197,8 +201,9 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->ntiles_max = (g->S + kTileTokens - 1) / kTileTokens;
     const size_t nt = (size_t)h->ntiles_max * g->E;
     // one allocation, carved in this order, each piece 256-byte aligned
-    const size_t counts[9] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
-                              (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1};
+    const size_t counts[10] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+                               (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1,
+                               (size_t)g->E * (((size_t)h->ntiles_max + 15) / 16) * 4};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -216,6 +221,8 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->row = carve<int32_t>(cur, counts[6]);
     h->idx = carve<int32_t>(cur, counts[7]);
     h->done = carve<unsigned>(cur, counts[8]);
+    h->cnt_stride = (h->ntiles_max + 15) & ~15;
+    h->tile_cnt = carve<uint8_t>(cur, (size_t)g->E * h->cnt_stride);
     if (cudaMemset(base, 0, bytes) != cudaSuccess) {
         cudaFree(base);
         delete h;

@@ -40,6 +40,7 @@ struct RouteParams {
 // Where the layout lives (the handle's workspace).
 struct LayoutArgs {
     uint32_t* tile_word;  // [ntiles][E]
+    uint8_t* tile_cnt;    // [E][cnt_stride], popc of tile_word, expert-major
     int32_t* tile_base;   // [ntiles][E]
     int32_t* cnt;         // [E]
     int32_t* off;         // [E+1]
@@ -47,6 +48,7 @@ struct LayoutArgs {
     int32_t* roff;        // [R+1]
     unsigned* done;       // CTAs finished (reset to 0 by the last one)
     int E, R, ntiles;
+    int cnt_stride;       // tiles per tile_cnt row, a multiple of 16
 };
 
 // What placing a pair into its receive row needs.

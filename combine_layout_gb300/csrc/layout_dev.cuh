@@ -19,77 +19,121 @@
 
 namespace moeep {
 
+// Shared memory the layout tail needs (ints): partial sums, warp sums,
+// per-expert counts and offsets.
+constexpr int kTailSmemInts = 1024 + 32 + 2 * (kMaxExperts + 1);
+
+// Sum of the four bytes of w.
+__device__ __forceinline__ int byte_sum(uint32_t w) { return (int)__dp4a(w, 0x01010101u, 0u); }
+
 // The last CTA of a layout-producing grid to finish computes, alone, the
 // column prefix over tiles, the per-expert counts and the offsets.  Every CTA
-// calls this after writing its tile words; only the last one returns true
-// after doing the work.  No CTA waits on another: the counter only tells the
-// CTA that arrives last that all words are written.
-__device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* s_scratch /*>= blockDim.x + 32 ints*/)
+// calls this after writing its tile words and per-tile counts; only the CTA
+// that arrives last does the work.  No CTA waits on another: the counter only
+// tells the CTA that arrives last that all tiles are written.
+// The one-byte counts are stored expert-major, tile_cnt[e][tile], so a
+// thread reads its run of tiles of one expert in 16-byte vectors, all in
+// flight at once; global memory is read once and written once, and
+// everything in between stays in shared memory.
+__device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* smem)
 {
+    // The barrier orders every thread's tile writes before thread 0's
+    // GPU-scope fence, which orders them before the arrival count (one fence
+    // per CTA: a fence in every thread costs microseconds).
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(a.done, 1u);
+        __threadfence();
+        s_last = (prev == gridDim.x - 1) ? 1 : 0;
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
 
     const int nthr = blockDim.x, tid = threadIdx.x;
     const int E = a.E, ntiles = a.ntiles;
-    // tpc threads share one expert column, each scanning a contiguous run of
-    // tiles; consecutive threads take consecutive columns (coalesced loads),
-    // and each thread keeps kBatch independent loads in flight.
-    constexpr int kBatch = 16;
+    int* s_part = smem;                 // [nthr]
+    int* s_warp = smem + nthr;          // [32]
+    int* s_cnt = s_warp + 32;           // [E]
+    int* s_off = s_cnt + kMaxExperts;   // [E + 1]
+
+    // tpc threads share one expert column, each taking a run of rp tiles
+    // (a multiple of 16: whole vectors)
+    constexpr int kVec = 8;  // 16-byte vectors held in registers (128 tiles)
     int tpc = 1;
     while (tpc * 2 * E <= nthr) tpc *= 2;
     const int cols_per_pass = nthr / tpc;
     const int col_in = tid % cols_per_pass, part = tid / cols_per_pass;
-    const int rp = (ntiles + tpc - 1) / tpc;
+    const int rp = (((ntiles + tpc - 1) / tpc) + 15) & ~15;
     const int r0 = min(part * rp, ntiles), r1 = min(r0 + rp, ntiles);
+    const int nv = (r1 - r0 + 15) / 16;
     for (int c0 = 0; c0 < E; c0 += cols_per_pass) {
         const int col = c0 + col_in;
-        const bool act = col < E && part < tpc;
+        const bool act = col < E;
+        const uint8_t* src = a.tile_cnt + (size_t)col * a.cnt_stride + r0;
+        uint4 v[kVec];
         int sum = 0;
-        if (act)
-            for (int rb = r0; rb < r1; rb += kBatch) {
-                uint32_t w[kBatch];
-#pragma unroll
-                for (int q = 0; q < kBatch; ++q)
-                    w[q] = (rb + q < r1) ? __ldcg(a.tile_word + (size_t)(rb + q) * E + col) : 0u;
-#pragma unroll
-                for (int q = 0; q < kBatch; ++q) sum += __popc(w[q]);
-            }
-        s_scratch[tid] = sum;
-        __syncthreads();
         if (act) {
-            int base = 0, total = 0;
-            for (int q = 0; q < tpc; ++q) {
-                const int v = s_scratch[q * cols_per_pass + col_in];
-                if (q < part) base += v;
-                total += v;
-            }
-            int run = base;
-            for (int rb = r0; rb < r1; rb += kBatch) {
-                uint32_t w[kBatch];
+            for (int b0 = 0; b0 < nv; b0 += kVec) {
 #pragma unroll
-                for (int q = 0; q < kBatch; ++q)
-                    w[q] = (rb + q < r1) ? __ldcg(a.tile_word + (size_t)(rb + q) * E + col) : 0u;
+                for (int i = 0; i < kVec; ++i)
+                    v[i] = (b0 + i < nv) ? __ldcg(reinterpret_cast<const uint4*>(src) + b0 + i)
+                                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int q = 0; q < kBatch; ++q) {
-                    if (rb + q < r1) a.tile_base[(size_t)(rb + q) * E + col] = run;
-                    run += __popc(w[q]);
+                for (int i = 0; i < kVec; ++i) {
+                    const int t0 = r0 + 16 * (b0 + i);
+                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int lim = r1 - (t0 + 4 * q);  // bytes of this word that count
+                        const uint32_t m = lim >= 4 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << (8 * lim)) - 1u);
+                        sum += byte_sum(w[q] & m);
+                    }
                 }
             }
-            if (part == 0) a.cnt[col] = total;
+        }
+        s_part[tid] = sum;
+        __syncthreads();
+        if (act) {
+            int run = 0, total = 0;
+            for (int q = 0; q < tpc; ++q) {
+                const int x = s_part[q * cols_per_pass + col_in];
+                if (q < part) run += x;
+                total += x;
+            }
+            for (int b0 = 0; b0 < nv; b0 += kVec) {
+                if (nv > kVec) {  // runs longer than the registers hold: read again
+#pragma unroll
+                    for (int i = 0; i < kVec; ++i)
+                        v[i] = (b0 + i < nv) ? __ldcg(reinterpret_cast<const uint4*>(src) + b0 + i)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                }
+                const int nvb = min(kVec, nv - b0);
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) {
+                    if (i >= nvb) break;  // only the vectors that hold tiles
+                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                    const int t0 = r0 + 16 * (b0 + i);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        if (t0 + q < r1) {
+                            a.tile_base[(size_t)(t0 + q) * E + col] = run;
+                            run += (int)((w[q >> 2] >> (8 * (q & 3))) & 0xffu);
+                        }
+                    }
+                }
+            }
+            if (part == 0) s_cnt[col] = total;
         }
         __syncthreads();
     }
 
-    // exclusive prefix of cnt over experts -> off; per-rank sums
+    // exclusive prefix of the counts over experts (shared memory only)
     const int per = (E + nthr - 1) / nthr;
     const int lo = min(tid * per, E), hi = min(lo + per, E);
     int sum = 0;
-    for (int e = lo; e < hi; ++e) sum += a.cnt[e];
+    for (int e = lo; e < hi; ++e) sum += s_cnt[e];
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     int incl = sum;
 #pragma unroll
@@ -97,33 +141,37 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
         const int n = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += n;
     }
-    int* s_warp = s_scratch + nthr;
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int v = lane < nwarps ? s_warp[lane] : 0;
+        int x = lane < nwarps ? s_warp[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += n;
+            const int n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
         }
-        if (lane < nwarps) s_warp[lane] = v;
+        if (lane < nwarps) s_warp[lane] = x;
     }
     __syncthreads();
     int run = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);
     for (int e = lo; e < hi; ++e) {
-        a.off[e] = run;
-        run += a.cnt[e];
+        s_off[e] = run;
+        run += s_cnt[e];
     }
-    if (tid == nthr - 1) a.off[E] = s_warp[nwarps - 1];
+    if (tid == nthr - 1) s_off[E] = s_warp[nwarps - 1];
     __syncthreads();
+    for (int e = tid; e < E; e += nthr) {
+        a.cnt[e] = s_cnt[e];
+        a.off[e] = s_off[e];
+    }
+    if (tid == 0) a.off[E] = s_off[E];
     const int L = E / a.R;
     for (int r = tid; r < a.R; r += nthr) {
-        a.roff[r] = a.off[r * L];
-        a.rcnt[r] = a.off[(r + 1) * L] - a.off[r * L];
+        a.roff[r] = s_off[r * L];
+        a.rcnt[r] = s_off[(r + 1) * L] - s_off[r * L];
     }
     if (tid == 0) {
-        a.roff[a.R] = a.off[E];
+        a.roff[a.R] = s_off[E];
         *a.done = 0u;  // ready for the next launch on this handle
     }
 }

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
                                                      float* __restrict__ topk_w, LayoutArgs la)
 {
     __shared__ uint32_t s_word[kMaxExperts];
-    __shared__ int s_scratch[1024 + 32];
+    __shared__ int s_scratch[kTailSmemInts];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < p.E; e += blockDim.x) s_word[e] = 0u;
     __syncthreads();
@@ -218,7 +218,11 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
         }
     }
     __syncthreads();
-    for (int e = tid; e < p.E; e += blockDim.x) la.tile_word[(size_t)tile * p.E + e] = s_word[e];
+    for (int e = tid; e < p.E; e += blockDim.x) {
+        const uint32_t wd = s_word[e];
+        la.tile_word[(size_t)tile * p.E + e] = wd;
+        la.tile_cnt[(size_t)e * la.cnt_stride + tile] = (uint8_t)__popc(wd);
+    }
     finish_layout_if_last(la, s_scratch);
 }
 
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
                                                           LayoutArgs la, volatile unsigned* err)
 {
     __shared__ uint32_t s_word[kMaxExperts];
-    __shared__ int s_scratch[256 + 32];
+    __shared__ int s_scratch[kTailSmemInts];
     const int tid = threadIdx.x, E = la.E;
     for (int e = tid; e < E; e += blockDim.x) s_word[e] = 0u;
     __syncthreads();
@@ -254,7 +258,11 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
         atomicOr(&s_word[e], 1u << tl);
     }
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) la.tile_word[(size_t)tile * E + e] = s_word[e];
+    for (int e = tid; e < E; e += blockDim.x) {
+        const uint32_t wd = s_word[e];
+        la.tile_word[(size_t)tile * E + e] = wd;
+        la.tile_cnt[(size_t)e * la.cnt_stride + tile] = (uint8_t)__popc(wd);
+    }
     finish_layout_if_last(la, s_scratch);
 }
 
