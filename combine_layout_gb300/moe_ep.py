@@ -54,6 +54,8 @@ def _load() -> ctypes.CDLL:
         "moe_ep_copy_layout": [P, P, P, P, P, P, P],
         "moe_ep_get_device_errors": [P, ctypes.POINTER(ctypes.c_uint32)],
         "moe_ep_clear_device_errors": [P],
+        "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
+                                       P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -179,3 +181,17 @@ def moe_ep_get_device_errors(group: int) -> int:
 
 def moe_ep_clear_device_errors(group: int) -> None:
     _check("moe_ep_clear_device_errors", _lib.moe_ep_clear_device_errors(ctypes.c_void_p(group)))
+
+
+def moe_ep_route_layout_static(scores, num_tokens: int, experts: int, ranks: int, mode: int,
+                               slots: int, topk: int, topk_idx, topk_w, row, cnt, off, rcnt, roff,
+                               num_groups: int = 1, topk_groups: int = 1, group_topk: int = 0,
+                               weight_mode: int = MOE_EP_W_SCORE_NORM, stream=None) -> None:
+    """Routing + layout into caller buffers with no device allocation (the
+    library's static scratch array); see include/moe_ep.h."""
+    opts = RouteOpts(topk, num_groups, topk_groups, group_topk, weight_mode)
+    _check("moe_ep_route_layout_static",
+           _lib.moe_ep_route_layout_static(_ptr(scores), num_tokens, experts, ranks, mode, slots,
+                                           ctypes.byref(opts), _ptr(topk_idx), _ptr(topk_w),
+                                           _ptr(row), _ptr(cnt), _ptr(off), _ptr(rcnt), _ptr(roff),
+                                           _stream(stream)))

@@ -183,6 +183,31 @@ MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* top
 MOE_EP_API int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* rcnt,
                        int32_t* roff, int32_t* row, moe_ep_stream_t stream);
 
+/* Routing + layout that allocates nothing, for callers that cannot allocate
+ * device memory themselves or through the library: a host whose memory pool or
+ * fixed memory plan owns every device byte and hands the library only
+ * pre-placed buffers.  (The source pages have no counterpart: there every
+ * rank allocates its communication buffers at group creation.)
+ * Computes what moe_ep_route followed by moe_ep_copy_layout computes on a
+ * handle of the same mode, experts, ranks and slots, with the same options:
+ * topk_idx [T][k], topk_w [T][k] (may be NULL), row [T][k], cnt [E],
+ * off [E+1], rcnt [R], roff [R+1], all device buffers owned by the caller.
+ * The layout's scratch lives in one static device array of 592 KiB that every
+ * GPU loading the library holds until exit; it is never allocated or freed.
+ * Capacity: ceil(num_tokens / 32) * experts <= 65536 (e.g. 8192 tokens with
+ * 256 experts); larger sizes return MOE_EP_ERR_OVERFLOW without launching.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the array: calls whose work overlaps on the GPU
+ * (different streams without ordering) race; calls on one stream do not.
+ * mode: MOE_EP_LL or MOE_EP_HT; slots: S for LL (>= num_tokens), ignored for HT.
+ * Asynchronous on `stream`. */
+MOE_EP_API int moe_ep_route_layout_static(const float* scores, int num_tokens, int experts,
+                                          int ranks, int mode, int slots,
+                                          const moe_ep_route_opts_t* opts, int32_t* topk_idx,
+                                          float* topk_w, int32_t* row, int32_t* cnt, int32_t* off,
+                                          int32_t* rcnt, int32_t* roff, moe_ep_stream_t stream);
+
 /* Read (host, no synchronisation) / clear the group's device-error word. */
 MOE_EP_API int moe_ep_get_device_errors(moe_ep_group_t g, uint32_t* bits);
 MOE_EP_API int moe_ep_clear_device_errors(moe_ep_group_t g);
