@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <chrono>
 #include <new>
 
 #include "common.cuh"
@@ -36,8 +37,12 @@ struct moe_ep_handle {
     int32_t* row;         // [max_tokens * max_topk]
     int32_t* idx;         // [max_tokens * max_topk], copy of the routing
     unsigned* done;       // layout CTA counter
-    // pinned host staging for the receive-count query: off[E+1] then rcnt[R]
-    int32_t* host_stage;
+    // counts published by the layout for the receive-count query (mapped
+    // pinned memory): off[E+1], rcnt[R], then the sequence number of the route
+    // that wrote them
+    int32_t* host_counts;
+    int32_t* host_counts_dev;  // device alias
+    unsigned seq;              // sequence number of the last HT route
     // state of the last route
     int routed;
     int rows_ready;       // row[] written for the last route
@@ -92,6 +97,8 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
     a.R = h->g->R;
     a.ntiles = (T + kTileTokens - 1) / kTileTokens;
     a.cnt_stride = h->cnt_stride;
+    a.host_out = nullptr;
+    a.seq = 0u;
     return a;
 }
 
@@ -229,13 +236,23 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
         return MOE_EP_ERR_CUDA;
     }
     void* hs = nullptr;
-    if (cudaHostAlloc(&hs, sizeof(int32_t) * (size_t)(g->E + 1 + g->R), cudaHostAllocDefault) !=
-        cudaSuccess) {
+    void* hs_dev = nullptr;
+    const size_t stage_bytes = sizeof(int32_t) * (size_t)(g->E + 1 + g->R + 1);
+    if (cudaHostAlloc(&hs, stage_bytes, cudaHostAllocMapped) != cudaSuccess) {
         cudaFree(base);
         delete h;
         return MOE_EP_ERR_CUDA;
     }
-    h->host_stage = (int32_t*)hs;
+    if (cudaHostGetDevicePointer(&hs_dev, hs, 0) != cudaSuccess) {
+        cudaFreeHost(hs);
+        cudaFree(base);
+        delete h;
+        return MOE_EP_ERR_CUDA;
+    }
+    memset(hs, 0, stage_bytes);
+    h->host_counts = (int32_t*)hs;
+    h->host_counts_dev = (int32_t*)hs_dev;
+    h->seq = 0u;
     h->routed = 0;
     h->rows_ready = 0;
     h->host_total = -1;
@@ -249,7 +266,7 @@ int moe_ep_destroy_handle(moe_ep_handle_t h)
     if (!h) return MOE_EP_ERR_INVALID;
     cudaError_t e = cudaDeviceSynchronize();
     cudaFree(h->tile_word);  // start of the single allocation
-    cudaFreeHost(h->host_stage);
+    cudaFreeHost(h->host_counts);
     h->g->handles -= 1;
     delete h;
     return cuda_status(e);
@@ -268,7 +285,12 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (T > g->S) return MOE_EP_ERR_OVERFLOW;
     if (T > 0 && !topk_idx) return MOE_EP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
-    const LayoutArgs la = layout_args(h, T);
+    LayoutArgs la = layout_args(h, T);
+    if (g->mode == MOE_EP_HT && T > 0) {
+        // the layout publishes the counts for the receive-count query
+        la.host_out = h->host_counts_dev;
+        la.seq = h->seq + 1u;
+    }
 
     if (T == 0) {
         // no pairs: counts and offsets are zero
@@ -307,6 +329,7 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
         st = cuda_status(launch_layout_bits(topk_idx, T, k, h->idx, la, g->err_dev, s));
     }
     if (st != MOE_EP_OK) return st;
+    if (la.host_out) h->seq = la.seq;
     h->routed = 1;
     h->rows_ready = 0;
     h->T = T;
@@ -331,22 +354,41 @@ int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_r
             for (int e = 0; e < g->E; ++e) per_expert[e] = g->S;
         return MOE_EP_OK;
     }
+    // HT: the layout kernel publishes off[] and rcnt[] into mapped host memory
+    // and then its route's sequence number; wait for that number only (not for
+    // the rest of the stream), checking the stream now and then for errors.
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemcpyAsync(h->host_stage, h->off, sizeof(int32_t) * (size_t)(g->E + 1),
-                                    cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(h->host_stage + g->E + 1, h->rcnt, sizeof(int32_t) * (size_t)g->R,
-                            cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return MOE_EP_ERR_CUDA;
+    const int E = g->E, R = g->R;
+    if (h->T > 0) {
+        volatile unsigned* seq_word = reinterpret_cast<volatile unsigned*>(h->host_counts + E + 1 + R);
+        const auto t0 = std::chrono::steady_clock::now();
+        for (uint64_t it = 1;; ++it) {
+            if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) == h->seq) break;
+            if ((it & 4095u) == 0u) {
+                const cudaError_t q = cudaStreamQuery(s);
+                if (q != cudaSuccess && q != cudaErrorNotReady) return MOE_EP_ERR_CUDA;
+                const bool idle = (q == cudaSuccess);
+                const bool late = std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10);
+                if (idle || late) {
+                    // everything on `stream` is done (or taking long): finish the
+                    // device's work, then the words must be there
+                    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_EP_ERR_CUDA;
+                    if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) != h->seq) return MOE_EP_ERR_CUDA;
+                    break;
+                }
+            }
+        }
+    }
     st = check_group(g);
     if (st != MOE_EP_OK) return st;
-    const int32_t* off = h->host_stage;
-    *total = off[g->E];
-    h->host_total = off[g->E];
-    if (per_rank) memcpy(per_rank, h->host_stage + g->E + 1, sizeof(int32_t) * (size_t)g->R);
+    const int32_t* off = h->host_counts;
+    const int64_t tot = (h->T > 0) ? off[E] : 0;
+    *total = tot;
+    h->host_total = tot;
+    if (per_rank)
+        for (int r = 0; r < R; ++r) per_rank[r] = (h->T > 0) ? off[E + 1 + r] : 0;
     if (per_expert)
-        for (int x = 0; x < g->E; ++x) per_expert[x] = off[x + 1] - off[x];
+        for (int x = 0; x < E; ++x) per_expert[x] = (h->T > 0) ? off[x + 1] - off[x] : 0;
     return MOE_EP_OK;
 }
 

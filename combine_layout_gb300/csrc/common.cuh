@@ -49,6 +49,11 @@ struct LayoutArgs {
     unsigned* done;       // CTAs finished (reset to 0 by the last one)
     int E, R, ntiles;
     int cnt_stride;       // tiles per tile_cnt row, a multiple of 16
+    // Optional publication of the counts to the host (mapped pinned memory,
+    // device alias): off[E+1], then rcnt[R], then the sequence number `seq`,
+    // written last, after a system-scope fence.  nullptr: no publication.
+    int32_t* host_out;
+    unsigned seq;
 };
 
 // What placing a pair into its receive row needs.

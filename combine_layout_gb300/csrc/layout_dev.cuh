@@ -174,6 +174,17 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
         a.roff[a.R] = s_off[E];
         *a.done = 0u;  // ready for the next launch on this handle
     }
+    if (a.host_out) {
+        // the host's copy of the counts (one host synchronisation of HT mode
+        // waits for these words, not for the rest of the stream)
+        for (int e = tid; e <= E; e += nthr) a.host_out[e] = s_off[e];
+        for (int r = tid; r < a.R; r += nthr) a.host_out[E + 1 + r] = s_off[(r + 1) * L] - s_off[r * L];
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence_system();
+            reinterpret_cast<volatile unsigned*>(a.host_out)[E + 1 + a.R] = a.seq;
+        }
+    }
 }
 
 // Receive row of pair (t, lane) for lanes < k of a warp (-1 for lanes >= k and

@@ -121,6 +121,8 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     la.R = ranks;
     la.ntiles = ntiles;
     la.cnt_stride = (ntiles + 15) & ~15;
+    la.host_out = nullptr;
+    la.seq = 0u;
 
     if (T == 0) {
         cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)experts, s);

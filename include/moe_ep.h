@@ -131,12 +131,16 @@ MOE_EP_API int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_toke
                  moe_ep_stream_t stream);
 
 /* Receive-token query ("核心功能函数": ncclEpHandleGetNumRecvTokens, used for
- * buffer sizing).  HT: copies the total receive rows and, if non-NULL, the
- * per-rank [R] and per-expert [E] counts to the host -- the one host
- * synchronisation of HT mode ("高吞吐模式": the CPU must learn the receive size);
- * it synchronises `stream`.  LL: returns the fixed capacity without any
- * synchronisation ("低延迟模式": no count exchange): total = E * S,
- * per_rank[r] = L * S, per_expert[e] = S.
+ * buffer sizing).  HT: returns the total receive rows and, if non-NULL, the
+ * per-rank [R] and per-expert [E] counts on the host -- the one host
+ * synchronisation of HT mode ("高吞吐模式": the CPU must learn the receive size).
+ * The layout of moe_ep_route publishes these counts into mapped host memory
+ * itself, so the call waits (host-side) for that layout only, not for work
+ * queued after it (a dispatch or combine already launched keeps running); on
+ * an error or a stall of more than 10 s it falls back to synchronising the
+ * device.  `stream` is only used for that check.  LL: returns the fixed
+ * capacity without any synchronisation ("低延迟模式": no count exchange):
+ * total = E * S, per_rank[r] = L * S, per_expert[e] = S.
  * total, per_rank, per_expert: host pointers (per_rank/per_expert may be NULL). */
 MOE_EP_API int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_rank,
                                int32_t* per_expert, moe_ep_stream_t stream);
