@@ -69,9 +69,13 @@ def measured_peak_gbs():
 
 
 def kernel_source_sha(kernel: str) -> str:
-    src = os.path.join(ROOT, "combine_layout_gb300", "csrc", f"{kernel}.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the shared headers it includes."""
+    csrc = os.path.join(ROOT, "combine_layout_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (f"{kernel}.cu", "common.cuh", "layout_dev.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
