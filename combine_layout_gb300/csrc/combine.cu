@@ -8,8 +8,9 @@
 //
 // out[t][h] = bf16_rn(fma(w_{k-1}, y_{k-1}, ... fma(w_1, y_1, fma(w_0, y_0, 0)))),
 // fp32 accumulation in fixed j order, so results do not depend on scheduling.
-// HBM-bound: k gathered row reads and one row write per token; every thread
-// issues the loads of all k rows for its 16-byte slice before accumulating.
+// HBM-bound: k gathered row reads and one row write per token; a CTA takes
+// one token at a time, every thread issuing the loads of all k rows for its
+// 16-byte slice before accumulating.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -40,8 +41,16 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8])
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Register budget per row count: enough CTAs per SM to keep the gathered rows
+// of many tokens in flight (k <= 8: 64 registers, 8 CTAs -- measured on the
+// bench shape 6.64 TB/s vs 6.29 TB/s with 5 CTAs; k <= 2: 32 registers).
+constexpr int combine_min_ctas(int kmax)
+{
+    return kmax <= 2 ? 16 : (kmax <= 4 ? 10 : (kmax <= 8 ? 8 : (kmax <= 16 ? 4 : 2)));
+}
+
 template <int KMAX>
-__global__ void __launch_bounds__(kThreads) combine_kernel(
+__global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kernel(
     const uint4* __restrict__ y, int T, int k, int nvec, const int32_t* __restrict__ row,
     const float* __restrict__ w, uint4* __restrict__ out)
 {
@@ -82,9 +91,9 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
 {
     if (T <= 0) return cudaSuccess;
     const int nvec = H / 8;
-    int blocks = T;
-    const int cap = sm_count * 16;
-    if (blocks > cap) blocks = cap;
+    // one CTA per token, at most 16 per SM (grid-stride beyond: small tokens
+    // then amortise the CTA launch)
+    const int blocks = T < sm_count * 16 ? T : sm_count * 16;
     const uint4* yy = (const uint4*)y;
     uint4* oo = (uint4*)out;
     if (k <= 1)

@@ -118,15 +118,34 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
                 const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+                // x / scale rounded to nearest (IEEE), by Markstein's method: with
+                // r = RN(1/scale), q0 = RN(x*r) is within 1 ulp of x/scale and
+                // RN(q0 + (x - q0*scale)*r) is exactly RN(x/scale), the remainder
+                // being exact in one fma -- provided nothing overflows or
+                // underflows, which 2^-80 <= amax <= 2^100 guarantees for every
+                // quotient whose e4m3 code depends on its low bits (smaller
+                // quotients all give the code 0).  Other blocks divide directly.
+                const bool fast = amax >= 0x1p-80f && amax <= 0x1p+100f;  // uniform per block
+                const float rs = fast ? __frcp_rn(scale) : 0.f;
+                float qt[8];
+                if (fast) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float q0 = __fmul_rn(f[i], rs);
+                        const float rem = __fmaf_rn(-q0, scale, f[i]);
+                        qt[i] = (f[i] == 0.f) ? f[i] : __fmaf_rn(rem, rs, q0);  // keep the sign of 0
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) qt[i] = __fdiv_rn(f[i], scale);
+                }
                 uint32_t packed[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                        make_float2(__fdiv_rn(f[4 * h + 0], scale), __fdiv_rn(f[4 * h + 1], scale)),
-                        __NV_SATFINITE, __NV_E4M3);
+                        make_float2(qt[4 * h + 0], qt[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
                     const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                        make_float2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)),
-                        __NV_SATFINITE, __NV_E4M3);
+                        make_float2(qt[4 * h + 2], qt[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
                     packed[h] = (uint32_t)lo | ((uint32_t)hi << 16);
                 }
                 q[u] = make_uint2(packed[0], packed[1]);

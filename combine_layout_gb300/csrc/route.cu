@@ -58,7 +58,38 @@ __device__ __forceinline__ void insert_desc(uint32_t (&t)[M], uint32_t x)
     }
 }
 
-template <int EPL, bool VEC>
+// Compare-exchange on (key desc, index asc): afterwards slot a holds the better.
+__device__ __forceinline__ void cx(uint32_t& ka, int& ia, uint32_t& kb, int& ib)
+{
+    const bool sw = kb > ka || (kb == ka && ib < ia);
+    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const int i0 = sw ? ib : ia, i1 = sw ? ia : ib;
+    ka = k0;
+    kb = k1;
+    ia = i0;
+    ib = i1;
+}
+
+// Sort a lane's candidates best first.  Eight: the optimal 19-comparator
+// network; other sizes: odd-even transposition (EPL rounds).
+template <int EPL>
+__device__ __forceinline__ void sort_desc(uint32_t (&k)[EPL], int (&ix)[EPL])
+{
+    if constexpr (EPL == 8) {
+        constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                                    {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                                    {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+        for (int c = 0; c < 19; ++c) cx(k[net[c][0]], ix[net[c][0]], k[net[c][1]], ix[net[c][1]]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < EPL; ++r)
+#pragma unroll
+            for (int i = r & 1; i + 1 < EPL; i += 2) cx(k[i], ix[i], k[i + 1], ix[i + 1]);
+    }
+}
+
+template <int EPL, bool VEC, int MG>
 __device__ __forceinline__ void route_token(const float* __restrict__ s, const RouteParams& p,
                                             int lane, int& out_idx, float& out_w)
 {
@@ -91,19 +122,22 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
     }
 
     uint32_t rem = inr;
-    if (p.limit) {
-        uint32_t top[kMaxGroupTopk];
+    uint32_t key0[EPL];  // the scores before any pick (renormalised softmax needs all)
 #pragma unroll
-        for (int q = 0; q < kMaxGroupTopk; ++q) top[q] = 0u;
+    for (int i = 0; i < EPL; ++i) key0[i] = key[i];
+    if (p.limit) {
+        uint32_t top[MG];  // the group's MG >= m best keys
+#pragma unroll
+        for (int q = 0; q < MG; ++q) top[q] = 0u;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if ((inr >> i) & 1u) insert_desc(top, key[i]);
         for (int o = 1; o < p.lpg; o <<= 1) {
-            uint32_t oth[kMaxGroupTopk];
+            uint32_t oth[MG];
 #pragma unroll
-            for (int q = 0; q < kMaxGroupTopk; ++q) oth[q] = __shfl_xor_sync(kFull, top[q], o);
+            for (int q = 0; q < MG; ++q) oth[q] = __shfl_xor_sync(kFull, top[q], o);
 #pragma unroll
-            for (int q = 0; q < kMaxGroupTopk; ++q) insert_desc(top, oth[q]);
+            for (int q = 0; q < MG; ++q) insert_desc(top, oth[q]);
         }
         // Group score: the exact sum of the group's m best scores.  For m <= 2
         // an fp32 two-sum gives it exactly as (hi, lo), and (hi, lo) pairs
@@ -111,7 +145,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         unsigned long long gk;
         if (p.m <= 2) {
             const float a = key_score(top[0]);
-            const float b = (p.m == 2) ? key_score(top[1]) : 0.f;
+            const float b = (p.m == 2) ? key_score(top[MG > 1 ? 1 : 0]) : 0.f;
             const float hi = __fadd_rn(b, a);
             float lo = 0.f;
             if (isfinite(hi)) {
@@ -122,7 +156,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         } else {
             double gsum = 0.0;
 #pragma unroll
-            for (int q = kMaxGroupTopk - 1; q >= 0; --q)
+            for (int q = MG - 1; q >= 0; --q)
                 if (q < p.m) gsum += (double)key_score(top[q]);
             gk = sum_key(gsum);
         }
@@ -134,23 +168,31 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         if (grp >= p.G || rank >= p.kg) rem = 0u;
     }
 
-    // k picks: largest key, then lowest index holding it
+    // k picks from lane-sorted candidates: the largest head key, then the
+    // lowest expert index holding it; the winning lane pops its head
+    int ix[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        if (!((rem >> i) & 1u)) key[i] = 0u;  // banned or absent: below every score
+        ix[i] = base + i;
+    }
+    sort_desc<EPL>(key, ix);
     int my_i = -1;
     uint32_t my_k = 0u, first_k = 0u;
     float den = 0.f;
     for (int j = 0; j < p.k; ++j) {
-        uint32_t bk = 0u;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (((rem >> i) & 1u) && key[i] > bk) {
-                bk = key[i];
-                bi = base + i;
-            }
-        const uint32_t mk = __reduce_max_sync(kFull, bk);
-        const uint32_t wi = __reduce_min_sync(kFull, (bk == mk) ? (uint32_t)bi : 0xffffffffu);
+        const uint32_t hk = key[0];
+        const uint32_t mk = __reduce_max_sync(kFull, hk);
+        const uint32_t wi = __reduce_min_sync(kFull, (hk == mk) ? (uint32_t)ix[0] : 0xffffffffu);
         const bool found = mk != 0u;
-        if (found && bk == mk && (uint32_t)bi == wi) rem &= ~(1u << (bi - base));
+        if (found && hk == mk && (uint32_t)ix[0] == wi) {
+#pragma unroll
+            for (int i = 0; i + 1 < EPL; ++i) {
+                key[i] = key[i + 1];
+                ix[i] = ix[i + 1];
+            }
+            key[EPL - 1] = 0u;
+        }
         if (lane == j) {
             my_i = found ? (int)wi : -1;  // not found is unreachable while kg * gs >= k
             my_k = mk;
@@ -174,12 +216,12 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         uint32_t mloc = 0u;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if ((inr >> i) & 1u) mloc = max(mloc, key[i]);
+            if ((inr >> i) & 1u) mloc = max(mloc, key0[i]);
         const float mx = key_score(__reduce_max_sync(kFull, mloc));
         float z = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if ((inr >> i) & 1u) z += expf(key_score(key[i]) - mx);
+            if ((inr >> i) & 1u) z += expf(key_score(key0[i]) - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
         const float pj = act ? __fdiv_rn(expf(my_v - mx), z) : 0.f;
@@ -191,7 +233,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
     out_w = w;
 }
 
-template <int EPL, bool VEC>
+template <int EPL, bool VEC, int MG>
 __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict__ scores, int T,
                                                      RouteParams p, int32_t* __restrict__ topk_idx,
                                                      int32_t* __restrict__ idx_copy,
@@ -208,7 +250,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
     if (t < T) {
         int e;
         float w;
-        route_token<EPL, VEC>(scores + (size_t)t * p.E, p, lane, e, w);
+        route_token<EPL, VEC, MG>(scores + (size_t)t * p.E, p, lane, e, w);
         if (lane < p.k) {
             const size_t q = (size_t)t * p.k + lane;
             topk_idx[q] = e;
@@ -266,17 +308,26 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
     finish_layout_if_last(la, s_scratch);
 }
 
+template <int EPL, bool VEC>
+void launch_route_mg(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
+                     int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
+{
+    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+    // the group list holds MG >= m keys (m = 1, 2: two; 3, 4: four)
+    if (!p.limit || p.m <= 2)
+        route_kernel<EPL, VEC, 2><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, la);
+    else
+        route_kernel<EPL, VEC, 4><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, la);
+}
+
 template <int EPL>
 void launch_route_epl(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
                       int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
-    const int ntiles = (T + kTileTokens - 1) / kTileTokens;
     if (EPL >= 4 && p.vec4)
-        route_kernel<EPL, (EPL >= 4)><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy,
-                                                              topk_w, la);
+        launch_route_mg<EPL, (EPL >= 4)>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     else
-        route_kernel<EPL, false><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w,
-                                                         la);
+        launch_route_mg<EPL, false>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
 }
 
 }  // namespace

@@ -104,7 +104,7 @@ class BoundStep:
 
     def __init__(self, p: EpPipeline, scores, x, y, num_tokens: int, num_groups: int = 1,
                  topk_groups: int = 1, group_topk: int = 0,
-                 weight_mode: int = ep.MOE_EP_W_SCORE_NORM, stream=None):
+                 weight_mode: int = ep.MOE_EP_W_SCORE_NORM, stream=None, out=None):
         import ctypes
 
         V = ctypes.c_void_p
@@ -126,7 +126,11 @@ class BoundStep:
         self._dispatch = (lib.moe_ep_dispatch, (h, ptr(x), int(p.fp8), ptr(p.recv_x),
                                                 ptr(p.recv_scale), ptr(p.recv_src),
                                                 ptr(p.recv_cnt), p.rows, s))
-        self._combine = (lib.moe_ep_combine, (h, ptr(y), ptr(p.topk_w), ptr(p.out), y.shape[0], s))
+        out = p.out if out is None else out
+        if not out.is_contiguous() or out.shape[0] < num_tokens:
+            raise ValueError("out must be contiguous with room for the tokens")
+        self.out = out
+        self._combine = (lib.moe_ep_combine, (h, ptr(y), ptr(p.topk_w), ptr(out), y.shape[0], s))
         self._query = (lib.moe_ep_get_num_recv_tokens,
                        (h, ctypes.byref(self._total),
                         ctypes.cast(self._per_rank, ctypes.c_void_p), None, s))

@@ -1,0 +1,59 @@
+"""Host logic of the benchmark's N > 1 path, on CPU with world-size-2 gloo:
+every rank runs an independent replica (tokens are independent), the job time
+is the slowest rank's, and the rate counts every rank's tokens."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, l = bench.rank_env()
+        assert (w, r, l) == (world, rank, rank)
+        ms = bench.reduce_max_over_ranks(10.0 + rank)   # rank 1 is the slowest
+        out[rank] = (ms, bench.whole_job_rate(4096, world, 100, ms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_rate_gloo():
+    world = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    assert out[0][0] == out[1][0] == 11.0
+    assert out[0][1] == pytest.approx(4096 * 2 * 100 / 11e-3)
+
+
+def test_single_process_defaults(monkeypatch):
+    import bench
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.rank_env() == (1, 0, 0)
+    assert bench.reduce_max_over_ranks(3.5) == 3.5
+    assert bench.whole_job_rate(4096, 1, 10, 2.0) == pytest.approx(4096 * 10 / 2e-3)
+
+
+def test_algorithmic_bytes_per_unit():
+    import bench
+    from combine_layout_gb300 import synth
+    w = synth.WORKLOADS["ht_prefill"]
+    ab = bench.algorithmic_bytes(w)
+    per_token = 2 * 7168 + 4 * 8 + 8 * (2 * 7168 + 4)
+    assert ab["dispatch"] == 4096 * per_token == 528_744_448
+    assert ab["combine"] == 4096 * (8 * (2 * 7168 + 8) + 2 * 7168)
+    ab8 = bench.algorithmic_bytes(synth.WORKLOADS["ht_prefill_fp8"])
+    assert ab8["dispatch"] == 4096 * (2 * 7168 + 32 + 8 * (7168 + 7168 // 32 + 4))

@@ -156,3 +156,70 @@ def test_fp8_conversion_sweep_all_bf16_values():
         assert np.array_equal(q[t], qo), t
     assert np.all(s[:-1] == 1.0)
     p.close()
+
+
+def _e4m3_values_and_midpoints():
+    vals = sorted({abs(oracle.e4m3_to_double(c)) for c in range(0x7F)})
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    return np.array(vals + mids)
+
+
+def test_fp8_quotients_on_ties_with_odd_scales():
+    """Blocks with amax = 448 * S * 2^j (S = 1..36) have the exact scale S * 2^j,
+    and elements x = m * S * 2^j put x / scale exactly on e4m3 values and
+    rounding midpoints (ties to even) for non-power-of-two scales; neighbours
+    one bf16 step away sit just off the ties.  Every byte must equal the
+    oracle's (IEEE fp32 division)."""
+    rng = np.random.default_rng(21)
+    targets = _e4m3_values_and_midpoints()
+    H = 7168
+    nblk = H // 128
+    T = 64
+    x = np.zeros((T, H), np.float32)
+    for t in range(T):
+        for b in range(nblk):
+            S = int(rng.integers(1, 37))
+            j = int(rng.integers(-60, 60))
+            scale = np.float32(S * 2.0 ** j)
+            blk = np.empty(128, np.float32)
+            blk[0] = np.float32(448.0 * S * 2.0 ** j)
+            m = rng.choice(targets, 127) * rng.choice([-1.0, 1.0], 127)
+            blk[1:] = (m * float(scale)).astype(np.float32)
+            x[t, b * 128:(b + 1) * 128] = blk
+    xb = synth.f32_to_bf16_bits(x)
+    # half the tokens: nudge every element one bf16 step up or down (off the ties)
+    nudge = rng.integers(-1, 2, xb.shape).astype(np.int32)
+    nudge[: T // 2] = 0
+    nudge[:, ::128] = 0                       # keep each block's amax element
+    xb = np.where(xb & 0x7FFF, (xb.astype(np.int32) + nudge).astype(np.uint16), xb)
+    _fp8_bytes_match_oracle(xb)
+
+
+def test_fp8_quotients_random_scales_both_paths():
+    """Random blocks whose amax spans 2^-130 .. 2^120 (both the reciprocal path
+    and the direct-division path), random signs and magnitudes inside blocks."""
+    rng = np.random.default_rng(22)
+    T, H = 256, 7168
+    e = rng.integers(-130, 121, (T, H // 128)).astype(np.float64)
+    mag = 2.0 ** (e[:, :, None] - rng.integers(0, 40, (T, H // 128, 128)))
+    x = (rng.uniform(0.5, 1.0, (T, H // 128, 128)) * mag * rng.choice([-1, 1], (T, H // 128, 128)))
+    x = np.clip(x, -3e38, 3e38).astype(np.float32).reshape(T, H)
+    x[::7, ::5] = -0.0
+    _fp8_bytes_match_oracle(synth.f32_to_bf16_bits(x))
+
+
+def _fp8_bytes_match_oracle(xb):
+    from combine_layout_gb300.pipeline import EpPipeline
+    T, H = xb.shape
+    p = EpPipeline(synth.MODE_HT, 8, 2, T, H, 1, fp8=True, device=DEV)
+    p.route_given(torch.zeros((T, 1), dtype=torch.int32, device=DEV))
+    p.dispatch(to_dev_bf16(xb, DEV))
+    torch.cuda.synchronize()
+    q = p.recv_x[:T].cpu().numpy()
+    s = p.recv_scale[:T].cpu().numpy()
+    for t in range(T):
+        qo, so = oracle.quant_row(xb[t])
+        assert np.array_equal(s[t], so), t
+        bad = np.nonzero(q[t] != qo)[0]
+        assert bad.size == 0, (t, bad[:4], q[t][bad[:4]], qo[bad[:4]])
+    p.close()
