@@ -14,6 +14,8 @@ Each wrapper follows a passage of the source pages (cited in moe_oracle.c):
               one fp32 scale per 128 elements ("高吞吐模式")
   combine  -- "NCCL EP 论文解读", "核心功能函数" (un-permute with the handle's routing
               state and reduce to token order); "高吞吐模式" (BF16 weighted sum)
+  node_layout -- "高吞吐模式": one copy per remote node (same-position GPU), then
+              forwarding to the GPUs holding the experts; the routing statistics
 """
 from __future__ import annotations
 
@@ -69,8 +71,10 @@ def _load():
     lib.orc_route.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P]
     lib.orc_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
     lib.orc_dispatch.argtypes = [P, i64, i32, i32, P, i64, i32, P, P, P]
+    lib.orc_node_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
     lib.orc_combine.argtypes = [P, i64, i32, P, P, i64, i32, P, i64, P]
-    for f in ("orc_quant_row", "orc_route", "orc_layout", "orc_dispatch", "orc_combine"):
+    for f in ("orc_quant_row", "orc_route", "orc_layout", "orc_dispatch", "orc_combine",
+              "orc_node_layout"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -148,6 +152,25 @@ def layout(topk_idx, experts: int, ranks: int, mode: int, slots: int = 0):
     st = _load().orc_layout(_p(idx), T, k, experts, ranks, mode, slots,
                             _p(cnt), _p(off), _p(rcnt), _p(roff), _p(row))
     return dict(cnt=cnt, off=off, rcnt=rcnt, roff=roff, row=row), st
+
+
+def node_layout(topk_idx, experts: int, ranks: int, nodes: int, src_node: int = 0):
+    """Node-level (two-hop) layout and the routing statistics.
+    Returns dict(cnt, off, src, mask, stats[4])."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    cnt = np.empty(nodes, np.int32)
+    off = np.empty(nodes + 1, np.int32)
+    rows = T * min(k, nodes)
+    src = np.full(max(rows, 1), -1, np.int32)
+    mask = np.zeros(max(rows, 1), np.uint32)
+    stats = np.zeros(4, np.int64)
+    st = _load().orc_node_layout(_p(idx), T, k, experts, ranks, nodes, src_node, _p(cnt), _p(off),
+                                 _p(src), _p(mask), _p(stats))
+    if st != OK:
+        raise ValueError(f"orc_node_layout status {st}")
+    n = int(off[-1])
+    return dict(cnt=cnt, off=off, src=src[:n], mask=mask[:n], stats=stats)
 
 
 def dispatch(x_bf16_bits, row, nrows: int, fp8: bool, recv_x=None, recv_scale=None,

@@ -310,6 +310,64 @@ int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode
 }
 
 /* ------------------------------------------------------------------------- */
+/* node-level (two-hop) layout                                                */
+/* ------------------------------------------------------------------------- */
+
+int orc_node_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int N, int src_node,
+                    int32_t* node_cnt, int32_t* node_off, int32_t* node_src, uint32_t* node_mask,
+                    int64_t* stats)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0 || N < 1 || R % N != 0 || N > 64 ||
+        R / N > 32 || src_node < 0 || src_node >= N)
+        return ORC_ERR_INVALID;
+    const int L = E / R, GPN = R / N;
+    uint32_t* mask = (uint32_t*)calloc((size_t)N, sizeof(uint32_t));
+    for (int n = 0; n < N; ++n) node_cnt[n] = 0;
+    for (int q = 0; q < 4; ++q) stats[q] = 0;
+    /* pass 1: per token, the GPUs it needs on every node; counts and statistics */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int n = 0; n < N; ++n) mask[n] = 0;
+        for (int j = 0; j < k; ++j) {
+            if (pair_kind(topk_idx + t * k, j, E) != 1) continue;
+            int e = topk_idx[t * k + j];
+            int gpu = e / L, n = gpu / GPN;
+            mask[n] |= 1u << (gpu % GPN);
+            if (n != src_node) stats[1] += 1;                 /* per expert */
+        }
+        for (int n = 0; n < N; ++n) {
+            if (!mask[n]) continue;
+            node_cnt[n] += 1;
+            stats[0] += 1;                                     /* nodes touched */
+            if (n != src_node) {
+                stats[3] += 1;                                 /* per node */
+                for (int g = 0; g < GPN; ++g) stats[2] += (mask[n] >> g) & 1u;   /* per GPU */
+            }
+        }
+    }
+    node_off[0] = 0;
+    for (int n = 0; n < N; ++n) node_off[n + 1] = node_off[n] + node_cnt[n];
+    /* pass 2: rows, node-major, tokens ascending */
+    int32_t* cursor = (int32_t*)calloc((size_t)N, sizeof(int32_t));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int n = 0; n < N; ++n) mask[n] = 0;
+        for (int j = 0; j < k; ++j) {
+            if (pair_kind(topk_idx + t * k, j, E) != 1) continue;
+            int gpu = topk_idx[t * k + j] / L;
+            mask[gpu / GPN] |= 1u << (gpu % GPN);
+        }
+        for (int n = 0; n < N; ++n) {
+            if (!mask[n]) continue;
+            int r = node_off[n] + cursor[n]++;
+            node_src[r] = (int32_t)t;
+            node_mask[r] = mask[n];
+        }
+    }
+    free(cursor);
+    free(mask);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* dispatch                                                                   */
 /* ------------------------------------------------------------------------- */
 

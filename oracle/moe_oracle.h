@@ -74,6 +74,22 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
 int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
                int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row);
 
+/* Node-level layout for two-hop dispatch ("NVSHMEM 与 DeepEP：GPU 发起的通信",
+ * section "高吞吐模式": a token goes once to every remote node that holds one of
+ * its experts, to the GPU in the same position, which forwards it over NVLink
+ * to the GPUs that hold the experts).  Experts are placed in contiguous
+ * blocks: gpu = e / (E/R), node = gpu / (R/N).
+ * Outputs: node_cnt [N] tokens touching node n, node_off [N+1], and per node
+ * row (node-major, tokens ascending) node_src = token, node_mask = bit g set
+ * when local GPU g of that node holds one of the token's experts.
+ * stats [4] (sums over tokens; -1 / invalid ids skipped, repeated experts
+ * counted once): distinct nodes touched (own node included), cross-node copies
+ * sent per expert, per distinct GPU, per distinct node -- the quantities of the
+ * page's routing simulation, with src_node as "own node". */
+int orc_node_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int N, int src_node,
+                    int32_t* node_cnt, int32_t* node_off, int32_t* node_src, uint32_t* node_mask,
+                    int64_t* stats);
+
 /* Dispatch: every (t, j) with row r >= 0 receives token t.
  * fp8 == 0: recv_x is bf16 [nrows][H] and recv_scale is unused.
  * fp8 != 0: recv_x is e4m3 [nrows][H], recv_scale fp32 [nrows][H/128].
