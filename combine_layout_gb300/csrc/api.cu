@@ -37,6 +37,11 @@ struct moe_ep_handle {
     int32_t* row;         // [max_tokens * max_topk]
     int32_t* idx;         // [max_tokens * max_topk], copy of the routing
     unsigned* done;       // layout CTA counter
+    // node-level layout workspace (nodes <= ranks)
+    uint32_t* ntile_word;  // [ntiles_max][R]
+    uint8_t* ntile_cnt;    // [R][cnt_stride]
+    int32_t* ntile_base;   // [ntiles_max][R]
+    unsigned* ndone;
     // counts published by the layout for the receive-count query (mapped
     // pinned memory): off[E+1], rcnt[R], then the sequence number of the route
     // that wrote them
@@ -208,9 +213,12 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->ntiles_max = (g->S + kTileTokens - 1) / kTileTokens;
     const size_t nt = (size_t)h->ntiles_max * g->E;
     // one allocation, carved in this order, each piece 256-byte aligned
-    const size_t counts[10] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+    const size_t ntn = (size_t)h->ntiles_max * g->R;
+    const size_t cstride = ((size_t)h->ntiles_max + 15) / 16 * 16;
+    const size_t counts[15] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
                                (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1,
-                               (size_t)g->E * (((size_t)h->ntiles_max + 15) / 16) * 4};
+                               (size_t)g->E * cstride / 4,
+                               ntn, (size_t)g->R * cstride / 4, ntn, 1, 0};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -230,6 +238,10 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->done = carve<unsigned>(cur, counts[8]);
     h->cnt_stride = (h->ntiles_max + 15) & ~15;
     h->tile_cnt = carve<uint8_t>(cur, (size_t)g->E * h->cnt_stride);
+    h->ntile_word = carve<uint32_t>(cur, ntn);
+    h->ntile_cnt = carve<uint8_t>(cur, (size_t)g->R * h->cnt_stride);
+    h->ntile_base = carve<int32_t>(cur, ntn);
+    h->ndone = carve<unsigned>(cur, 1);
     if (cudaMemset(base, 0, bytes) != cudaSuccess) {
         cudaFree(base);
         delete h;
@@ -440,6 +452,59 @@ int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* 
     if (st != MOE_EP_OK) return st;
     return cuda_status(launch_combine(y, h->T, g->H, h->k, h->row, topk_w, out, g->sm_count,
                                       (cudaStream_t)stream));
+}
+
+int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* node_cnt,
+                       int32_t* node_off, int32_t* node_src, uint32_t* node_mask,
+                       int64_t node_rows, int64_t* stats, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    const int N = num_nodes;
+    if (N < 1 || N > g->R || g->R % N != 0 || g->R / N > 32 || src_node < 0 || src_node >= N)
+        return MOE_EP_ERR_INVALID;
+    if (!node_cnt || !node_off) return MOE_EP_ERR_INVALID;
+    const int T = h->T, k = h->k;
+    if (T > 0 && (!node_src || !node_mask)) return MOE_EP_ERR_INVALID;
+    if (node_rows < (int64_t)T * (k < N ? k : N)) return MOE_EP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (stats) e = cudaMemsetAsync(stats, 0, 4 * sizeof(int64_t), s);
+    if (e == cudaSuccess && T == 0) {
+        e = cudaMemsetAsync(node_cnt, 0, sizeof(int32_t) * (size_t)N, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(node_off, 0, sizeof(int32_t) * (size_t)(N + 1), s);
+        return cuda_status(e);
+    }
+    if (e != cudaSuccess) return MOE_EP_ERR_CUDA;
+    NodeArgs a;
+    a.idx = h->idx;
+    a.T = T;
+    a.k = k;
+    a.E = g->E;
+    a.L = g->L;
+    a.gpn = g->R / N;
+    a.N = N;
+    a.src = src_node;
+    LayoutArgs la;
+    la.tile_word = h->ntile_word;
+    la.tile_cnt = h->ntile_cnt;
+    la.tile_base = h->ntile_base;
+    la.cnt = node_cnt;
+    la.off = node_off;
+    la.rcnt = node_cnt;  // one "rank" per node: the same sums
+    la.roff = node_off;
+    la.done = h->ndone;
+    la.E = N;
+    la.R = N;
+    la.ntiles = (T + kTileTokens - 1) / kTileTokens;
+    la.cnt_stride = h->cnt_stride;
+    la.host_out = nullptr;
+    la.seq = 0u;
+    return cuda_status(launch_node_layout(a, la, reinterpret_cast<unsigned long long*>(stats),
+                                          node_src, node_mask, g->sm_count, s));
 }
 
 int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff,

@@ -65,6 +65,16 @@ struct RowArgs {
     int T, k, E, S, mode;
 };
 
+// What the node-level layout needs.
+struct NodeArgs {
+    const int32_t* idx;  // handle copy of topk_idx [T][k]
+    int T, k, E;
+    int L;               // experts per GPU (rank)
+    int gpn;             // GPUs per node
+    int N;               // nodes
+    int src;             // source node
+};
+
 // Router: one warp per token, one 32-token tile per CTA.  Writes topk_idx
 // (caller's and the handle's copy), topk_w, the tile words, and -- in the
 // last CTA to finish -- tile_base, cnt, off, rcnt, roff.
@@ -84,6 +94,11 @@ cudaError_t launch_rowmap(const RowArgs& ra, int32_t* row, int sm_count, cudaStr
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
                             const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s);
+
+// Node-level layout (node counts, offsets, rows with GPU masks) and the
+// routing statistics (stats may be null; otherwise 4 sums, accumulated).
+cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned long long* stats,
+                               int32_t* node_src, uint32_t* node_mask, int sm_count, cudaStream_t s);
 
 // Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,

@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "moe_ep_copy_layout": [P, P, P, P, P, P, P],
         "moe_ep_get_device_errors": [P, ctypes.POINTER(ctypes.c_uint32)],
         "moe_ep_clear_device_errors": [P],
+        "moe_ep_node_layout": [P, I, I, P, P, P, P, I64, P, P],
         "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
                                        P, P, P],
     }
@@ -170,6 +171,17 @@ def moe_ep_copy_layout(handle: int, cnt=None, off=None, rcnt=None, roff=None, ro
     _check("moe_ep_copy_layout",
            _lib.moe_ep_copy_layout(ctypes.c_void_p(handle), _ptr(cnt), _ptr(off), _ptr(rcnt),
                                    _ptr(roff), _ptr(row), _stream(stream)))
+
+
+def moe_ep_node_layout(handle: int, num_nodes: int, src_node: int, node_cnt, node_off,
+                       node_src, node_mask, stats=None, node_rows: int | None = None,
+                       stream=None) -> None:
+    if node_rows is None:
+        node_rows = node_src.shape[0] if node_src is not None else 0
+    _check("moe_ep_node_layout",
+           _lib.moe_ep_node_layout(ctypes.c_void_p(handle), num_nodes, src_node, _ptr(node_cnt),
+                                   _ptr(node_off), _ptr(node_src), _ptr(node_mask), node_rows,
+                                   _ptr(stats), _stream(stream)))
 
 
 def moe_ep_get_device_errors(group: int) -> int:

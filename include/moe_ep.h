@@ -180,6 +180,31 @@ MOE_EP_API int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* 
 MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
                    int64_t recv_rows, moe_ep_stream_t stream);
 
+/* Node-level layout of the last route, for two-hop dispatch ("NVSHMEM 与 DeepEP：
+ * GPU 发起的通信", section "高吞吐模式": a token is sent once to every remote node
+ * that holds one of its experts -- to the GPU in the same position -- which
+ * forwards it over NVLink to the GPUs holding the experts).  The R ranks form
+ * num_nodes nodes of R / num_nodes GPUs (contiguous), GPU g of node n being
+ * rank n * (R / num_nodes) + g.
+ * node_cnt  device int32 [N]: tokens touching node n.
+ * node_off  device int32 [N+1]: exclusive prefix of node_cnt.
+ * node_src  device int32 [node_rows]: token of each node row; rows are
+ *           node-major with tokens ascending.
+ * node_mask device uint32 [node_rows]: bit g set when GPU g of the row's node
+ *           holds one of the token's experts (the forwarding set).
+ * node_rows capacity of node_src / node_mask: at least T * min(k, N).
+ * stats     device int64 [4] or NULL, overwritten: sums over tokens of (0) nodes
+ *           touched, own node included; cross-node copies (1) per expert,
+ *           (2) per distinct GPU, (3) per distinct node, src_node being the
+ *           source GPU's node -- the quantities of the page's routing simulation.
+ * Masked (-1), invalid and repeated expert ids are skipped as in the layout.
+ * Errors: MOE_EP_ERR_INVALID for N not dividing R, R / N > 32, src_node
+ * outside [0, N), too small node_rows, or no preceding moe_ep_route. */
+MOE_EP_API int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node,
+                                  int32_t* node_cnt, int32_t* node_off, int32_t* node_src,
+                                  uint32_t* node_mask, int64_t node_rows, int64_t* stats,
+                                  moe_ep_stream_t stream);
+
 /* Copy the handle's layout to caller buffers (device or host pointers; NULL
  * skips an item): cnt [E], off [E+1], rcnt [R], roff [R+1], row [T][k] with -1
  * for pairs without a row.  Asynchronous for device destinations; host
