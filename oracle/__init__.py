@@ -70,11 +70,13 @@ def _load():
     lib.orc_quant_row.argtypes = [P, i32, P, P]
     lib.orc_route.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P]
     lib.orc_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
+    lib.orc_layout_aligned.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P, P, P, P]
+    lib.orc_dequant_rows.argtypes = [P, P, i64, i32, P, i64, P]
     lib.orc_dispatch.argtypes = [P, i64, i32, i32, P, i64, i32, P, P, P]
     lib.orc_node_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
     lib.orc_combine.argtypes = [P, i64, i32, P, P, i64, i32, P, i64, P]
     for f in ("orc_quant_row", "orc_route", "orc_layout", "orc_dispatch", "orc_combine",
-              "orc_node_layout"):
+              "orc_node_layout", "orc_layout_aligned", "orc_dequant_rows"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -140,8 +142,9 @@ def route(scores, k: int, num_groups: int = 1, topk_groups: int = 1,
     return idx, w
 
 
-def layout(topk_idx, experts: int, ranks: int, mode: int, slots: int = 0):
-    """Counts, offsets and the row map. Returns (dict, status)."""
+def layout(topk_idx, experts: int, ranks: int, mode: int, slots: int = 0, align: int = 1):
+    """Counts, offsets and the row map (HT expert blocks padded to `align` rows).
+    Returns (dict, status)."""
     idx = _c(topk_idx, np.int32)
     T, k = idx.shape
     cnt = np.empty(experts, np.int32)
@@ -149,9 +152,26 @@ def layout(topk_idx, experts: int, ranks: int, mode: int, slots: int = 0):
     rcnt = np.empty(ranks, np.int32)
     roff = np.empty(ranks + 1, np.int32)
     row = np.empty((T, k), np.int32)
-    st = _load().orc_layout(_p(idx), T, k, experts, ranks, mode, slots,
-                            _p(cnt), _p(off), _p(rcnt), _p(roff), _p(row))
+    if align == 1:
+        st = _load().orc_layout(_p(idx), T, k, experts, ranks, mode, slots,
+                                _p(cnt), _p(off), _p(rcnt), _p(roff), _p(row))
+    else:
+        st = _load().orc_layout_aligned(_p(idx), T, k, experts, ranks, mode, slots, align,
+                                        _p(cnt), _p(off), _p(rcnt), _p(roff), _p(row))
     return dict(cnt=cnt, off=off, rcnt=rcnt, roff=roff, row=row), st
+
+
+def dequant_rows(q, scale, rows) -> np.ndarray:
+    """bf16 bits of float(q) * scale (fp32 product) for the listed rows, zeros elsewhere."""
+    q = _c(q, np.uint8)
+    nrows, H = q.shape
+    sc = _c(scale, np.float32)
+    r = _c(rows, np.int64).reshape(-1)
+    y = np.zeros((nrows, H), np.uint16)
+    st = _load().orc_dequant_rows(_p(q), _p(sc), nrows, H, _p(r), r.size, _p(y))
+    if st != OK:
+        raise ValueError(f"orc_dequant_rows status {st}")
+    return y
 
 
 def node_layout(topk_idx, experts: int, ranks: int, nodes: int, src_node: int = 0):

@@ -265,7 +265,14 @@ static int pair_kind(const int32_t* idx_row, int j, int E)
 int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
                int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row)
 {
-    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0) return ORC_ERR_INVALID;
+    return orc_layout_aligned(topk_idx, T, k, E, R, mode, S, 1, cnt, off, rcnt, roff, row);
+}
+
+int orc_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
+                       int align, int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff,
+                       int32_t* row)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0 || align < 1) return ORC_ERR_INVALID;
     if (mode != ORC_MODE_LL && mode != ORC_MODE_HT) return ORC_ERR_INVALID;
     if (mode == ORC_MODE_LL && S < 1) return ORC_ERR_INVALID;
     const int L = E / R;
@@ -280,13 +287,12 @@ int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode
             if (kind == 1) cnt[topk_idx[t * k + j]] += 1;
         }
     off[0] = 0;
-    for (int e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+    for (int e = 0; e < E; ++e) off[e + 1] = off[e] + (cnt[e] + align - 1) / align * align;
     for (int r = 0; r < R; ++r) {
         rcnt[r] = 0;
         for (int l = 0; l < L; ++l) rcnt[r] += cnt[r * L + l];
     }
-    roff[0] = 0;
-    for (int r = 0; r < R; ++r) roff[r + 1] = roff[r] + rcnt[r];
+    for (int r = 0; r <= R; ++r) roff[r] = off[r * L];
 
     /* Pass 2: each pair's place, tokens of one expert in ascending order. */
     int32_t* cursor = (int32_t*)calloc((size_t)E, sizeof(int32_t));
@@ -307,6 +313,27 @@ int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode
         }
     free(cursor);
     return status;
+}
+
+/* ------------------------------------------------------------------------- */
+/* dequantisation                                                             */
+/* ------------------------------------------------------------------------- */
+
+int orc_dequant_rows(const uint8_t* q, const float* scale, int64_t nrows, int H,
+                     const int64_t* rows, int64_t nlist, uint16_t* y)
+{
+    if (H <= 0 || H % 128 != 0) return ORC_ERR_INVALID;
+    const int nb = H / 128;
+    for (int64_t i = 0; i < nlist; ++i) {
+        const int64_t r = rows[i];
+        if (r < 0 || r >= nrows) return ORC_ERR_INVALID;
+        for (int h = 0; h < H; ++h) {
+            const float v = (float)orc_e4m3_to_double(q[r * H + h]);   /* exact */
+            const float p = v * scale[r * nb + h / 128];                /* fp32 product */
+            y[r * H + h] = orc_bf16_from_double((double)p);             /* one bf16 rounding */
+        }
+    }
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------- */

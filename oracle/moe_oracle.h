@@ -74,6 +74,22 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
 int orc_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
                int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff, int32_t* row);
 
+/* The same layout with every HT expert block padded to a multiple of `align`
+ * rows (so a grouped GEMM takes whole row tiles per expert; "NCCL EP 论文解读",
+ * "Tensor Layouts": the expert-major layout feeds the GEMM directly):
+ * off[e+1] = off[e] + roundup(cnt[e], align); rows off[e] + rank; roff[r] =
+ * off[r * L]; cnt and rcnt stay the actual counts.  align = 1 is orc_layout. */
+int orc_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R, int mode, int S,
+                       int align, int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff,
+                       int32_t* row);
+
+/* Dequantise FP8 receive rows to bf16: y = bf16_rn(float(q) * scale), the
+ * product rounded to fp32 first (fp32 dequantisation, bf16 storage).
+ * q [nrows][H] e4m3, scale [nrows][H/128], y [nrows][H] bf16 bits; only the
+ * rows listed in `rows` (nlist entries) are written. */
+int orc_dequant_rows(const uint8_t* q, const float* scale, int64_t nrows, int H,
+                     const int64_t* rows, int64_t nlist, uint16_t* y);
+
 /* Node-level layout for two-hop dispatch ("NVSHMEM 与 DeepEP：GPU 发起的通信",
  * section "高吞吐模式": a token goes once to every remote node that holds one of
  * its experts, to the GPU in the same position, which forwards it over NVLink

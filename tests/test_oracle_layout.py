@@ -137,3 +137,48 @@ def test_page_ll_buffer_arithmetic():
 def test_layout_rejects_bad_shapes(orc, mode):
     L, st = orc.layout(np.zeros((4, 2), np.int32), 10, 3, mode, 8)
     assert st == orc.ERR_INVALID
+
+
+def test_aligned_layout_pads_expert_blocks(orc):
+    T, E, R, k = 300, 32, 8, 4
+    idx = _routed(orc, T, E, k)
+    base, _ = orc.layout(idx, E, R, orc.MODE_HT)
+    for align in (1, 2, 8, 128):
+        L, st = orc.layout(idx, E, R, orc.MODE_HT, align=align)
+        assert st == orc.OK
+        pad = (base["cnt"] + align - 1) // align * align
+        assert np.array_equal(L["cnt"], base["cnt"]) and np.array_equal(L["rcnt"], base["rcnt"])
+        assert np.array_equal(np.diff(L["off"]), pad) and np.all(L["off"] % align == 0)
+        assert np.array_equal(L["roff"], L["off"][:: E // R])
+        # same in-expert ranks, shifted to the padded block starts
+        e = idx
+        assert np.array_equal(L["row"] - L["off"][e], base["row"] - base["off"][e])
+    L1, _ = orc.layout(idx, E, R, orc.MODE_HT, align=1)
+    assert all(np.array_equal(L1[k_], base[k_]) for k_ in base)
+
+
+def test_dequant_closed_forms_and_torch(orc):
+    import torch
+    rng = np.random.default_rng(9)
+    q = rng.integers(0, 256, (6, 256)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x12                   # no NaN codes
+    sc = np.ones((6, 2), np.float32)
+    y = orc.dequant_rows(q, sc, [0, 2])
+    # scale 1: every e4m3 value is a bf16 value, exactly
+    want = synth.f32_to_bf16_bits(np.array([orc.e4m3_to_double(c) for c in q[0]], np.float32))
+    assert np.array_equal(y[0], want) and np.all(y[1] == 0)
+    # library routine: torch's fp8 decode, fp32 product, bf16 round to nearest even
+    sc = (rng.random((6, 2)) * 2.0 ** rng.integers(-20, 20, (6, 2))).astype(np.float32)
+    y = orc.dequant_rows(q, sc, range(6))
+    tq = torch.from_numpy(q).view(torch.float8_e4m3fn).float()
+    ts = torch.from_numpy(np.repeat(sc, 128, axis=1))
+    want = (tq * ts).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y, want)
+    # round trip: dequant(quant(x)) within half an e4m3 ulp of x
+    x = synth.tokens_bf16(rng, 1, 256)[0]
+    qq, ss = orc.quant_row(x)
+    yy = synth.bf16_bits_to_f32(orc.dequant_rows(qq[None], ss[None], [0])[0]).astype(np.float64)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    amax = np.repeat(np.abs(xf).reshape(2, 128).max(1), 128)
+    assert np.all(np.abs(yy - xf) <= np.maximum(np.abs(xf) * 2 ** -4, amax / 448 * 2 ** -10) * 1.01
+                  + np.abs(xf) * 2 ** -8)
