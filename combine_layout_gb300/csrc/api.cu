@@ -43,8 +43,8 @@ struct moe_ep_handle {
     int32_t* ntile_base;   // [ntiles_max][R]
     unsigned* ndone;
     // counts published by the layout for the receive-count query (mapped
-    // pinned memory): off[E+1], rcnt[R], then the sequence number of the route
-    // that wrote them
+    // pinned memory): off[E+1], rcnt[R], cnt[E], then the sequence number of
+    // the route that wrote them
     int32_t* host_counts;
     int32_t* host_counts_dev;  // device alias
     unsigned seq;              // sequence number of the last HT route
@@ -53,6 +53,7 @@ struct moe_ep_handle {
     int rows_ready;       // row[] written for the last route
     int T, k;
     int64_t host_total;   // total rows known on the host (-1: not queried)
+    int align;            // HT expert blocks padded to a multiple of align rows
 };
 
 namespace {
@@ -84,7 +85,7 @@ int64_t required_rows(const moe_ep_handle* h)
     const moe_ep_group* g = h->g;
     if (g->mode == MOE_EP_LL) return (int64_t)g->E * g->S;
     if (h->host_total >= 0) return h->host_total;
-    return (int64_t)h->T * h->k;
+    return (int64_t)h->T * h->k + (int64_t)g->E * (h->align - 1);
 }
 
 LayoutArgs layout_args(const moe_ep_handle* h, int T)
@@ -104,6 +105,7 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
     a.cnt_stride = h->cnt_stride;
     a.host_out = nullptr;
     a.seq = 0u;
+    a.align = h->align;
     return a;
 }
 
@@ -249,7 +251,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     }
     void* hs = nullptr;
     void* hs_dev = nullptr;
-    const size_t stage_bytes = sizeof(int32_t) * (size_t)(g->E + 1 + g->R + 1);
+    const size_t stage_bytes = sizeof(int32_t) * (size_t)(g->E + 1 + g->R + g->E + 1);
     if (cudaHostAlloc(&hs, stage_bytes, cudaHostAllocMapped) != cudaSuccess) {
         cudaFree(base);
         delete h;
@@ -268,6 +270,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->routed = 0;
     h->rows_ready = 0;
     h->host_total = -1;
+    h->align = 1;
     g->handles += 1;
     *out = h;
     return MOE_EP_OK;
@@ -372,7 +375,7 @@ int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_r
     cudaStream_t s = (cudaStream_t)stream;
     const int E = g->E, R = g->R;
     if (h->T > 0) {
-        volatile unsigned* seq_word = reinterpret_cast<volatile unsigned*>(h->host_counts + E + 1 + R);
+        volatile unsigned* seq_word = reinterpret_cast<volatile unsigned*>(h->host_counts + E + 1 + R + E);
         const auto t0 = std::chrono::steady_clock::now();
         for (uint64_t it = 1;; ++it) {
             if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) == h->seq) break;
@@ -400,7 +403,7 @@ int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_r
     if (per_rank)
         for (int r = 0; r < R; ++r) per_rank[r] = (h->T > 0) ? off[E + 1 + r] : 0;
     if (per_expert)
-        for (int x = 0; x < E; ++x) per_expert[x] = (h->T > 0) ? off[x + 1] - off[x] : 0;
+        for (int x = 0; x < E; ++x) per_expert[x] = (h->T > 0) ? off[E + 1 + R + x] : 0;
     return MOE_EP_OK;
 }
 
@@ -454,6 +457,33 @@ int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* 
                                       (cudaStream_t)stream));
 }
 
+int moe_ep_set_row_align(moe_ep_handle_t h, int align)
+{
+    if (!h || align < 1 || align > 1024 || (align & (align - 1)) != 0) return MOE_EP_ERR_INVALID;
+    if (h->g->mode != MOE_EP_HT && align != 1) return MOE_EP_ERR_INVALID;
+    h->align = align;
+    return MOE_EP_OK;
+}
+
+int moe_ep_dequant(moe_ep_handle_t h, const void* recv_q, const float* recv_scale, void* y,
+                   int64_t recv_rows, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed) return MOE_EP_ERR_INVALID;
+    if (g->H % 128 != 0) return MOE_EP_ERR_INVALID;
+    if (recv_rows < required_rows(h)) return MOE_EP_ERR_INVALID;
+    if (h->T == 0) return MOE_EP_OK;
+    if (!recv_q || !recv_scale || !y || !aligned16(recv_q) || !aligned16(y) ||
+        ((uintptr_t)recv_scale & 3u))
+        return MOE_EP_ERR_INVALID;
+    return cuda_status(launch_dequant(h->cnt, h->off, g->E, g->S, g->mode, g->H,
+                                      (const uint8_t*)recv_q, recv_scale, y, g->sm_count,
+                                      (cudaStream_t)stream));
+}
+
 int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* node_cnt,
                        int32_t* node_off, int32_t* node_src, uint32_t* node_mask,
                        int64_t node_rows, int64_t* stats, moe_ep_stream_t stream)
@@ -503,6 +533,7 @@ int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* 
     la.cnt_stride = h->cnt_stride;
     la.host_out = nullptr;
     la.seq = 0u;
+    la.align = 1;
     return cuda_status(launch_node_layout(a, la, reinterpret_cast<unsigned long long*>(stats),
                                           node_src, node_mask, g->sm_count, s));
 }

@@ -49,9 +49,10 @@ struct LayoutArgs {
     unsigned* done;       // CTAs finished (reset to 0 by the last one)
     int E, R, ntiles;
     int cnt_stride;       // tiles per tile_cnt row, a multiple of 16
+    int align;            // expert blocks padded to a multiple of align rows (1: none)
     // Optional publication of the counts to the host (mapped pinned memory,
-    // device alias): off[E+1], then rcnt[R], then the sequence number `seq`,
-    // written last, after a system-scope fence.  nullptr: no publication.
+    // device alias): off[E+1], rcnt[R], cnt[E], then the sequence number
+    // `seq`, written last, after a system-scope fence.  nullptr: none.
     int32_t* host_out;
     unsigned seq;
 };
@@ -99,6 +100,12 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
 // routing statistics (stats may be null; otherwise 4 sums, accumulated).
 cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned long long* stats,
                                int32_t* node_src, uint32_t* node_mask, int sm_count, cudaStream_t s);
+
+// Receive-side dequantisation of the rows the layout defines:
+// y = bf16_rn(float(q) * scale) (fp32 product).
+cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S, int mode, int H,
+                           const uint8_t* q, const float* scale, void* y, int sm_count,
+                           cudaStream_t s);
 
 // Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,

@@ -129,11 +129,12 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
         __syncthreads();
     }
 
-    // exclusive prefix of the counts over experts (shared memory only)
+    // exclusive prefix of the (padded) counts over experts (shared memory only)
+    const int al = a.align;
     const int per = (E + nthr - 1) / nthr;
     const int lo = min(tid * per, E), hi = min(lo + per, E);
     int sum = 0;
-    for (int e = lo; e < hi; ++e) sum += s_cnt[e];
+    for (int e = lo; e < hi; ++e) sum += (s_cnt[e] + al - 1) / al * al;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     int incl = sum;
 #pragma unroll
@@ -156,7 +157,7 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
     int run = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);
     for (int e = lo; e < hi; ++e) {
         s_off[e] = run;
-        run += s_cnt[e];
+        run += (s_cnt[e] + al - 1) / al * al;
     }
     if (tid == nthr - 1) s_off[E] = s_warp[nwarps - 1];
     __syncthreads();
@@ -167,8 +168,11 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
     if (tid == 0) a.off[E] = s_off[E];
     const int L = E / a.R;
     for (int r = tid; r < a.R; r += nthr) {
+        int c = 0;
+        for (int l = 0; l < L; ++l) c += s_cnt[r * L + l];
         a.roff[r] = s_off[r * L];
-        a.rcnt[r] = s_off[(r + 1) * L] - s_off[r * L];
+        a.rcnt[r] = c;
+        if (a.host_out) a.host_out[E + 1 + r] = c;
     }
     if (tid == 0) {
         a.roff[a.R] = s_off[E];
@@ -178,11 +182,11 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
         // the host's copy of the counts (one host synchronisation of HT mode
         // waits for these words, not for the rest of the stream)
         for (int e = tid; e <= E; e += nthr) a.host_out[e] = s_off[e];
-        for (int r = tid; r < a.R; r += nthr) a.host_out[E + 1 + r] = s_off[(r + 1) * L] - s_off[r * L];
+        for (int e = tid; e < E; e += nthr) a.host_out[E + 1 + a.R + e] = s_cnt[e];
         __syncthreads();
         if (tid == 0) {
             __threadfence_system();
-            reinterpret_cast<volatile unsigned*>(a.host_out)[E + 1 + a.R] = a.seq;
+            reinterpret_cast<volatile unsigned*>(a.host_out)[E + 1 + a.R + E] = a.seq;
         }
     }
 }

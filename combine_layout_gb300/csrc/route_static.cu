@@ -123,6 +123,7 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     la.cnt_stride = (ntiles + 15) & ~15;
     la.host_out = nullptr;
     la.seq = 0u;
+    la.align = 1;
 
     if (T == 0) {
         cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)experts, s);

@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
         "moe_ep_get_device_errors": [P, ctypes.POINTER(ctypes.c_uint32)],
         "moe_ep_clear_device_errors": [P],
         "moe_ep_node_layout": [P, I, I, P, P, P, P, I64, P, P],
+        "moe_ep_set_row_align": [P, I],
+        "moe_ep_dequant": [P, P, P, P, I64, P],
         "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
                                        P, P, P],
     }
@@ -171,6 +173,19 @@ def moe_ep_copy_layout(handle: int, cnt=None, off=None, rcnt=None, roff=None, ro
     _check("moe_ep_copy_layout",
            _lib.moe_ep_copy_layout(ctypes.c_void_p(handle), _ptr(cnt), _ptr(off), _ptr(rcnt),
                                    _ptr(roff), _ptr(row), _stream(stream)))
+
+
+def moe_ep_set_row_align(handle: int, align: int) -> None:
+    _check("moe_ep_set_row_align", _lib.moe_ep_set_row_align(ctypes.c_void_p(handle), align))
+
+
+def moe_ep_dequant(handle: int, recv_q, recv_scale, y, recv_rows: int | None = None,
+                   stream=None) -> None:
+    if recv_rows is None:
+        recv_rows = recv_q.shape[0]
+    _check("moe_ep_dequant",
+           _lib.moe_ep_dequant(ctypes.c_void_p(handle), _ptr(recv_q), _ptr(recv_scale), _ptr(y),
+                               recv_rows, _stream(stream)))
 
 
 def moe_ep_node_layout(handle: int, num_nodes: int, src_node: int, node_cnt, node_off,

@@ -14,13 +14,17 @@ from . import moe_ep as ep
 
 class EpPipeline:
     def __init__(self, mode: int, experts: int, ranks: int, max_tokens: int, hidden: int,
-                 topk: int, fp8: bool = False, device: str | int = "cuda"):
+                 topk: int, fp8: bool = False, device: str | int = "cuda", align: int = 1):
         self.mode, self.E, self.R, self.S, self.H, self.k = mode, experts, ranks, max_tokens, hidden, topk
         self.fp8 = fp8
         self.device = torch.device(device)
         self.group = ep.moe_ep_create_group(mode, experts, ranks, max_tokens, hidden)
         self.handle = ep.moe_ep_create_handle(self.group, topk)
-        self.rows = experts * max_tokens if mode == ep.MOE_EP_LL else max_tokens * topk
+        if align != 1:
+            ep.moe_ep_set_row_align(self.handle, align)
+        self.align = align
+        self.rows = (experts * max_tokens if mode == ep.MOE_EP_LL
+                     else max_tokens * topk + experts * (align - 1))
         dev = self.device
         self.topk_idx = torch.empty((max_tokens, topk), dtype=torch.int32, device=dev)
         self.topk_w = torch.empty((max_tokens, topk), dtype=torch.float32, device=dev)
@@ -61,6 +65,13 @@ class EpPipeline:
             out = self.out
         ep.moe_ep_combine(self.handle, y, topk_w, out, y.shape[0], stream)
         return out[: self.T]
+
+    def dequant(self, y=None, stream=None):
+        """bf16 expert-major rows from the FP8 receive buffers (defined rows only)."""
+        if y is None:
+            y = torch.zeros((self.rows, self.H), dtype=torch.bfloat16, device=self.device)
+        ep.moe_ep_dequant(self.handle, self.recv_x, self.recv_scale, y, self.rows, stream)
+        return y
 
     def layout(self, stream=None) -> dict:
         dev = self.device

@@ -180,6 +180,31 @@ MOE_EP_API int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* 
 MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
                    int64_t recv_rows, moe_ep_stream_t stream);
 
+/* Pad every HT expert block of the receive layout to a multiple of `align`
+ * rows (a power of two, 1..1024; 1 = dense, the default) for the routes that
+ * follow: expert e's rows become off[e] .. off[e] + cnt[e] with off[e] a
+ * multiple of align, so a grouped GEMM takes whole row tiles per expert
+ * ("NCCL EP 论文解读", "Tensor Layouts": the expert-major layout feeds the GEMM
+ * directly).  Padding rows are never written.  The receive-count query then
+ * returns total = off[E] (the rows to allocate) and the actual per-rank and
+ * per-expert counts; before a query, dispatch and combine require
+ * T * k + E * (align - 1) receive rows.  LL layouts are slot-aligned already:
+ * only align = 1 is accepted in LL mode.  Host only, no synchronisation. */
+MOE_EP_API int moe_ep_set_row_align(moe_ep_handle_t h, int align);
+
+/* Receive-side dequantisation of an FP8 dispatch: for every row the last
+ * route's layout defines (HT: expert blocks without their padding; LL: slots
+ * below each expert's count), y[row] = bf16_rn(float(q[row]) * scale), the
+ * product in fp32, one scale per 128 elements -- the bf16 expert-major input
+ * of an expert GEMM.  Rows the layout does not define are left untouched.
+ * recv_q device e4m3 [recv_rows][H] (16-byte aligned), recv_scale device fp32
+ * [recv_rows][H/128], y device bf16 [recv_rows][H] (16-byte aligned, may not
+ * overlap recv_q).  No host synchronisation: the rows are enumerated on the
+ * device from the counts.  Errors: MOE_EP_ERR_INVALID for H % 128 != 0,
+ * misaligned pointers, too few rows, or no preceding moe_ep_route. */
+MOE_EP_API int moe_ep_dequant(moe_ep_handle_t h, const void* recv_q, const float* recv_scale,
+                              void* y, int64_t recv_rows, moe_ep_stream_t stream);
+
 /* Node-level layout of the last route, for two-hop dispatch ("NVSHMEM 与 DeepEP：
  * GPU 发起的通信", section "高吞吐模式": a token is sent once to every remote node
  * that holds one of its experts -- to the GPU in the same position -- which
