@@ -80,18 +80,32 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
         const uint4* qr = q + (size_t)row * nvq;
         const float* sr = scale + (size_t)row * nbk;
         uint4* yr = y + (size_t)row * (H / 8);
-        for (int v = lane; v < nvq; v += 32) {
-            const uint4 w = __ldg(qr + v);
-            const float s = __ldg(sr + (v >> 3));  // 16 values lie in one 128-block
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-            uint32_t o[8];
+        constexpr int U = 7;  // vectors in flight per lane
+        for (int v0 = lane; v0 < nvq; v0 += 32 * U) {
+            uint4 w[U];
+            float s[U];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                o[2 * c] = dequant_pair((uint16_t)(u[c] & 0xffffu), s);
-                o[2 * c + 1] = dequant_pair((uint16_t)(u[c] >> 16), s);
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < nvq) {
+                    w[u] = __ldg(qr + v);
+                    s[u] = __ldg(sr + (v >> 3));  // 16 values lie in one 128-block
+                }
             }
-            yr[2 * v] = make_uint4(o[0], o[1], o[2], o[3]);
-            yr[2 * v + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= nvq) break;
+                const uint32_t x[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    o[2 * c] = dequant_pair((uint16_t)(x[c] & 0xffffu), s[u]);
+                    o[2 * c + 1] = dequant_pair((uint16_t)(x[c] >> 16), s[u]);
+                }
+                yr[2 * v] = make_uint4(o[0], o[1], o[2], o[3]);
+                yr[2 * v + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
         }
     }
 }
