@@ -54,6 +54,8 @@ struct moe_ep_handle {
     int T, k;
     int64_t host_total;   // total rows known on the host (-1: not queried)
     int align;            // HT expert blocks padded to a multiple of align rows
+    cudaEvent_t sent;     // recorded after a send-only dispatch / combine
+    int has_sent;
 };
 
 namespace {
@@ -267,6 +269,13 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->host_counts = (int32_t*)hs;
     h->host_counts_dev = (int32_t*)hs_dev;
     h->seq = 0u;
+    if (cudaEventCreateWithFlags(&h->sent, cudaEventDisableTiming) != cudaSuccess) {
+        cudaFreeHost(hs);
+        cudaFree(base);
+        delete h;
+        return MOE_EP_ERR_CUDA;
+    }
+    h->has_sent = 0;
     h->routed = 0;
     h->rows_ready = 0;
     h->host_total = -1;
@@ -282,6 +291,7 @@ int moe_ep_destroy_handle(moe_ep_handle_t h)
     cudaError_t e = cudaDeviceSynchronize();
     cudaFree(h->tile_word);  // start of the single allocation
     cudaFreeHost(h->host_counts);
+    cudaEventDestroy(h->sent);
     h->g->handles -= 1;
     delete h;
     return cuda_status(e);
@@ -455,6 +465,37 @@ int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* 
     if (st != MOE_EP_OK) return st;
     return cuda_status(launch_combine(y, h->T, g->H, h->k, h->row, topk_w, out, g->sm_count,
                                       (cudaStream_t)stream));
+}
+
+int moe_ep_dispatch_send(moe_ep_handle_t h, const void* x, int fp8, void* recv_x,
+                         float* recv_scale, int32_t* recv_src, int32_t* recv_cnt,
+                         int64_t recv_rows, moe_ep_stream_t send_stream)
+{
+    int st = moe_ep_dispatch(h, x, fp8, recv_x, recv_scale, recv_src, recv_cnt, recv_rows,
+                             send_stream);
+    if (st != MOE_EP_OK) return st;
+    if (cudaEventRecord(h->sent, (cudaStream_t)send_stream) != cudaSuccess) return MOE_EP_ERR_CUDA;
+    h->has_sent = 1;
+    return MOE_EP_OK;
+}
+
+int moe_ep_combine_send(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
+                        int64_t recv_rows, moe_ep_stream_t send_stream)
+{
+    int st = moe_ep_combine(h, y, topk_w, out, recv_rows, send_stream);
+    if (st != MOE_EP_OK) return st;
+    if (cudaEventRecord(h->sent, (cudaStream_t)send_stream) != cudaSuccess) return MOE_EP_ERR_CUDA;
+    h->has_sent = 1;
+    return MOE_EP_OK;
+}
+
+int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    int st = check_group(h->g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->has_sent) return MOE_EP_OK;
+    return cuda_status(cudaStreamWaitEvent((cudaStream_t)stream, h->sent, 0));
 }
 
 int moe_ep_set_row_align(moe_ep_handle_t h, int align)

@@ -56,6 +56,9 @@ def _load() -> ctypes.CDLL:
         "moe_ep_clear_device_errors": [P],
         "moe_ep_node_layout": [P, I, I, P, P, P, P, I64, P, P],
         "moe_ep_set_row_align": [P, I],
+        "moe_ep_dispatch_send": [P, P, I, P, P, P, P, I64, P],
+        "moe_ep_combine_send": [P, P, P, P, I64, P],
+        "moe_ep_complete": [P, P],
         "moe_ep_dequant": [P, P, P, P, I64, P],
         "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
                                        P, P, P],
@@ -173,6 +176,29 @@ def moe_ep_copy_layout(handle: int, cnt=None, off=None, rcnt=None, roff=None, ro
     _check("moe_ep_copy_layout",
            _lib.moe_ep_copy_layout(ctypes.c_void_p(handle), _ptr(cnt), _ptr(off), _ptr(rcnt),
                                    _ptr(roff), _ptr(row), _stream(stream)))
+
+
+def moe_ep_dispatch_send(handle: int, x, fp8: bool, recv_x, recv_scale=None, recv_src=None,
+                         recv_cnt=None, recv_rows: int | None = None, stream=None) -> None:
+    if recv_rows is None:
+        recv_rows = recv_x.shape[0]
+    _check("moe_ep_dispatch_send",
+           _lib.moe_ep_dispatch_send(ctypes.c_void_p(handle), _ptr(x), int(bool(fp8)),
+                                     _ptr(recv_x), _ptr(recv_scale), _ptr(recv_src),
+                                     _ptr(recv_cnt), recv_rows, _stream(stream)))
+
+
+def moe_ep_combine_send(handle: int, y, topk_w, out, recv_rows: int | None = None,
+                        stream=None) -> None:
+    if recv_rows is None:
+        recv_rows = y.shape[0]
+    _check("moe_ep_combine_send",
+           _lib.moe_ep_combine_send(ctypes.c_void_p(handle), _ptr(y), _ptr(topk_w), _ptr(out),
+                                    recv_rows, _stream(stream)))
+
+
+def moe_ep_complete(handle: int, stream=None) -> None:
+    _check("moe_ep_complete", _lib.moe_ep_complete(ctypes.c_void_p(handle), _stream(stream)))
 
 
 def moe_ep_set_row_align(handle: int, align: int) -> None:

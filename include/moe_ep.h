@@ -180,6 +180,26 @@ MOE_EP_API int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* 
 MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
                    int64_t recv_rows, moe_ep_stream_t stream);
 
+/* Staged execution ("NCCL EP 论文解读", items "核心功能函数" and "send_only与双
+ * buffer": with send_only a dispatch or combine only starts its transfer and
+ * returns, ncclEpComplete later finishes the receive, and two micro-batches on
+ * two handles -- double buffers -- overlap one's transfer with the other's
+ * expert computation; "低延迟模式" on the DeepEP page: the LL hook).
+ * moe_ep_dispatch_send / moe_ep_combine_send: the same work as moe_ep_dispatch
+ * / moe_ep_combine, enqueued on `send_stream`, after which the handle records
+ * its completion event.  moe_ep_complete: makes `stream` wait (on the device,
+ * no host synchronisation) until the handle's last send-only operation has
+ * finished; a no-op if the handle never sent.  On one GPU the data lands in
+ * the receive rows when the send kernel ends, so completion is that kernel's
+ * end; no kernel ever spins.  With LL mode (no host synchronisation anywhere)
+ * route, sends, completes and combines can be captured into a CUDA graph. */
+MOE_EP_API int moe_ep_dispatch_send(moe_ep_handle_t h, const void* x, int fp8, void* recv_x,
+                                    float* recv_scale, int32_t* recv_src, int32_t* recv_cnt,
+                                    int64_t recv_rows, moe_ep_stream_t send_stream);
+MOE_EP_API int moe_ep_combine_send(moe_ep_handle_t h, const void* y, const float* topk_w,
+                                   void* out, int64_t recv_rows, moe_ep_stream_t send_stream);
+MOE_EP_API int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream);
+
 /* Pad every HT expert block of the receive layout to a multiple of `align`
  * rows (a power of two, 1..1024; 1 = dense, the default) for the routes that
  * follow: expert e's rows become off[e] .. off[e] + cnt[e] with off[e] a
