@@ -59,7 +59,8 @@ def test_aligned_layout_and_round_trip(name, T, align):
 
 
 @pytest.mark.parametrize("name,T,align", [("ht_prefill_fp8", 300, 128), ("skewed", 1000, 1),
-                                          ("ll_decode", 128, 1), ("ll_decode", 45, 1)])
+                                          ("ll_decode", 128, 1), ("ll_decode", 45, 1),
+                                          ("ht_prefill_fp8", 4096, 1)])
 def test_dequant_matches_oracle(name, T, align):
     w = synth.WORKLOADS[name].with_tokens(T, slots=synth.WORKLOADS[name].slots or None)
     inp = synth.make_inputs(w)
