@@ -27,9 +27,8 @@ struct moe_ep_handle {
     int ntiles_max;
     // device workspace
     uint32_t* tile_word;  // [ntiles_max][E]
-    uint8_t* tile_cnt;    // [E][cnt_stride]
-    int cnt_stride;       // ntiles_max rounded up to 16
-    int32_t* tile_base;   // [ntiles_max][E]
+    uint8_t* tile_cnt;    // [ngroups_max][E][16]
+    int32_t* grp_base;    // [ngroups_max][E]
     int32_t* cnt;         // [E]
     int32_t* off;         // [E+1]
     int32_t* rcnt;        // [R]
@@ -39,8 +38,8 @@ struct moe_ep_handle {
     unsigned* done;       // layout CTA counter
     // node-level layout workspace (nodes <= ranks)
     uint32_t* ntile_word;  // [ntiles_max][R]
-    uint8_t* ntile_cnt;    // [R][cnt_stride]
-    int32_t* ntile_base;   // [ntiles_max][R]
+    uint8_t* ntile_cnt;    // [ngroups_max][R][16]
+    int32_t* ngrp_base;    // [ngroups_max][R]
     unsigned* ndone;
     // counts published by the layout for the receive-count query (mapped
     // pinned memory): off[E+1], rcnt[R], cnt[E], then the sequence number of
@@ -95,7 +94,7 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
     LayoutArgs a;
     a.tile_word = h->tile_word;
     a.tile_cnt = h->tile_cnt;
-    a.tile_base = h->tile_base;
+    a.grp_base = h->grp_base;
     a.cnt = h->cnt;
     a.off = h->off;
     a.rcnt = h->rcnt;
@@ -104,7 +103,6 @@ LayoutArgs layout_args(const moe_ep_handle* h, int T)
     a.E = h->g->E;
     a.R = h->g->R;
     a.ntiles = (T + kTileTokens - 1) / kTileTokens;
-    a.cnt_stride = h->cnt_stride;
     a.host_out = nullptr;
     a.seq = 0u;
     a.align = h->align;
@@ -116,7 +114,8 @@ RowArgs row_args(const moe_ep_handle* h)
     RowArgs a;
     a.idx = h->idx;
     a.tile_word = h->tile_word;
-    a.tile_base = h->tile_base;
+    a.tile_cnt = h->tile_cnt;
+    a.grp_base = h->grp_base;
     a.off = h->off;
     a.T = h->T;
     a.k = h->k;
@@ -219,10 +218,11 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     // one allocation, carved in this order, each piece 256-byte aligned
     const size_t ntn = (size_t)h->ntiles_max * g->R;
     const size_t cstride = ((size_t)h->ntiles_max + 15) / 16 * 16;
-    const size_t counts[15] = {nt, nt, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+    const size_t ngrp = cstride / 16;
+    const size_t counts[15] = {nt, ngrp * g->E, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
                                (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1,
                                (size_t)g->E * cstride / 4,
-                               ntn, (size_t)g->R * cstride / 4, ntn, 1, 0};
+                               ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1, 0};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -232,7 +232,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     }
     char* cur = (char*)base;
     h->tile_word = carve<uint32_t>(cur, counts[0]);
-    h->tile_base = carve<int32_t>(cur, counts[1]);
+    h->grp_base = carve<int32_t>(cur, counts[1]);
     h->cnt = carve<int32_t>(cur, counts[2]);
     h->off = carve<int32_t>(cur, counts[3]);
     h->rcnt = carve<int32_t>(cur, counts[4]);
@@ -240,11 +240,10 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->row = carve<int32_t>(cur, counts[6]);
     h->idx = carve<int32_t>(cur, counts[7]);
     h->done = carve<unsigned>(cur, counts[8]);
-    h->cnt_stride = (h->ntiles_max + 15) & ~15;
-    h->tile_cnt = carve<uint8_t>(cur, (size_t)g->E * h->cnt_stride);
+    h->tile_cnt = carve<uint8_t>(cur, (size_t)g->E * cstride);
     h->ntile_word = carve<uint32_t>(cur, ntn);
-    h->ntile_cnt = carve<uint8_t>(cur, (size_t)g->R * h->cnt_stride);
-    h->ntile_base = carve<int32_t>(cur, ntn);
+    h->ntile_cnt = carve<uint8_t>(cur, (size_t)g->R * cstride);
+    h->ngrp_base = carve<int32_t>(cur, counts[12]);
     h->ndone = carve<unsigned>(cur, 1);
     if (cudaMemset(base, 0, bytes) != cudaSuccess) {
         cudaFree(base);
@@ -562,7 +561,7 @@ int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* 
     LayoutArgs la;
     la.tile_word = h->ntile_word;
     la.tile_cnt = h->ntile_cnt;
-    la.tile_base = h->ntile_base;
+    la.grp_base = h->ngrp_base;
     la.cnt = node_cnt;
     la.off = node_off;
     la.rcnt = node_cnt;  // one "rank" per node: the same sums
@@ -571,7 +570,6 @@ int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* 
     la.E = N;
     la.R = N;
     la.ntiles = (T + kTileTokens - 1) / kTileTokens;
-    la.cnt_stride = h->cnt_stride;
     la.host_out = nullptr;
     la.seq = 0u;
     la.align = 1;

@@ -40,16 +40,20 @@ struct RouteParams {
 // Where the layout lives (the handle's workspace).
 struct LayoutArgs {
     uint32_t* tile_word;  // [ntiles][E]
-    uint8_t* tile_cnt;    // [E][cnt_stride], popc of tile_word, expert-major
-    int32_t* tile_base;   // [ntiles][E]
+    uint8_t* tile_cnt;    // [ngroups][E][16], popc of tile_word (groups of 16 tiles)
+    int32_t* grp_base;    // [ngroups][E], pairs before each group of 16 tiles
     int32_t* cnt;         // [E]
     int32_t* off;         // [E+1]
     int32_t* rcnt;        // [R]
     int32_t* roff;        // [R+1]
     unsigned* done;       // CTAs finished (reset to 0 by the last one)
     int E, R, ntiles;
-    int cnt_stride;       // tiles per tile_cnt row, a multiple of 16
     int align;            // expert blocks padded to a multiple of align rows (1: none)
+    // Work split of the last CTA, set on the host for the launch's block size
+    // (tail_planned in layout_dev.cuh): experts per rank, column-pass columns,
+    // parts and groups per part, experts per prefix thread, prefix threads,
+    // threads that take part at all.
+    int L, cols, parts, rg, per, nact, nwork;
     // Optional publication of the counts to the host (mapped pinned memory,
     // device alias): off[E+1], rcnt[R], cnt[E], then the sequence number
     // `seq`, written last, after a system-scope fence.  nullptr: none.
@@ -61,7 +65,8 @@ struct LayoutArgs {
 struct RowArgs {
     const int32_t* idx;        // handle copy of topk_idx [T][k]
     const uint32_t* tile_word;
-    const int32_t* tile_base;
+    const uint8_t* tile_cnt;
+    const int32_t* grp_base;
     const int32_t* off;
     int T, k, E, S, mode;
 };
@@ -77,8 +82,8 @@ struct NodeArgs {
 };
 
 // Router: one warp per token, one 32-token tile per CTA.  Writes topk_idx
-// (caller's and the handle's copy), topk_w, the tile words, and -- in the
-// last CTA to finish -- tile_base, cnt, off, rcnt, roff.
+// (caller's and the handle's copy), topk_w, the tile words and byte counts,
+// and -- in the last CTA to finish -- grp_base, cnt, off, rcnt, roff.
 cudaError_t launch_route(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
                          int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s);
 

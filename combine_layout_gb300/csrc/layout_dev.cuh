@@ -8,185 +8,248 @@
 // "低延迟模式" on the DeepEP page: fixed slots per (rank, local expert).
 //
 // Representation: tokens are grouped in tiles of 32; word tile_word[tile][e]
-// has bit i set when token tile*32 + i chose expert e.  Then
-//   cnt[e]            = sum over tiles of popc(word)
-//   tile_base[tile][e] = pairs of expert e in earlier tiles
-//   rank(t, e)         = tile_base[t/32][e] + popc(word & bits below t%32)
+// has bit i set when token tile*32 + i chose expert e.  Tiles are grouped 16
+// at a time, and the byte counts popc(word) of one expert in one group form
+// one 16-byte vector: tile_cnt[g][e][j] = popc(tile_word[16g + j][e]).  Then
+//   cnt[e]           = sum of expert e's byte counts
+//   grp_base[g][e]   = pairs of expert e in the groups before g
+//   rank(t, e)       = grp_base[g][e] + sum of tile_cnt[g][e][0 .. j)
+//                      + popc(word & bits below t%32),   tile = t/32 = 16g + j,
 // is the number of earlier tokens that chose e, i.e. the stable in-expert rank.
+// The last CTA of the producing grid writes E bases per 512 tokens (not per
+// 32): one CTA's work is the serial part of the layout.
 #pragma once
 
 #include "common.cuh"
 
 namespace moeep {
 
-// Shared memory the layout tail needs (ints): partial sums, warp sums,
+constexpr int kGroupTiles = 16;
+
+// Shared memory the layout tail needs (ints): per-part sums, warp sums,
 // per-expert counts and offsets.
-constexpr int kTailSmemInts = 1024 + 32 + 2 * (kMaxExperts + 1);
+constexpr int kTailSmemInts = 1024 + 32 + 2 * kMaxExperts;
+
+// Byte offset of tile `tile`'s count for column c (ncols columns).
+__device__ __forceinline__ size_t tile_cnt_index(int tile, int c, int ncols)
+{
+    return ((size_t)(tile / kGroupTiles) * ncols + c) * kGroupTiles + (tile % kGroupTiles);
+}
 
 // Sum of the four bytes of w.
 __device__ __forceinline__ int byte_sum(uint32_t w) { return (int)__dp4a(w, 0x01010101u, 0u); }
 
+// Mask of the low n bytes of a word (n clamped to [0, 4]).
+__device__ __forceinline__ uint32_t low_bytes(int n)
+{
+    return n >= 4 ? 0xffffffffu : (n <= 0 ? 0u : (1u << (8 * n)) - 1u);
+}
+
+// Sum of the first n of the 16 bytes in v.
+__device__ __forceinline__ int vec_byte_sum(const uint4& v, int n)
+{
+    if (n >= 16) {
+        const unsigned ones = 0x01010101u;
+        return (int)__dp4a(v.w, ones, __dp4a(v.z, ones, __dp4a(v.y, ones, __dp4a(v.x, ones, 0u))));
+    }
+    return byte_sum(v.x & low_bytes(n)) + byte_sum(v.y & low_bytes(n - 4)) +
+           byte_sum(v.z & low_bytes(n - 8)) + byte_sum(v.w & low_bytes(n - 12));
+}
+
+// Pairs of column c (an expert, or a node) in the tiles before `tile`.
+__device__ __forceinline__ int pairs_before_tile(const uint8_t* tile_cnt, const int32_t* grp_base,
+                                                 int ncols, int c, int tile)
+{
+    const int g = tile / kGroupTiles;
+    const size_t q = (size_t)g * ncols + c;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(tile_cnt) + q);
+    return __ldg(grp_base + q) + vec_byte_sum(v, tile - g * kGroupTiles);
+}
+
+// Vectors (groups) a thread of the last CTA keeps in flight.
+constexpr int kTailVec = 8;
+
+// The last CTA's work split for a launch of nthr threads per CTA (host side).
+// A column (expert) is split into parts only when it has more than kTailVec
+// groups; only as many warps as the work needs take part.
+inline LayoutArgs tail_planned(LayoutArgs a, int nthr)
+{
+    const int ngroups = (a.ntiles + kGroupTiles - 1) / kGroupTiles;
+    a.L = a.E / a.R;
+    a.cols = a.E < nthr ? a.E : nthr;
+    int parts = (ngroups + kTailVec - 1) / kTailVec;
+    if (parts > nthr / a.cols) parts = nthr / a.cols;
+    a.parts = parts < 1 ? 1 : parts;
+    a.rg = (ngroups + a.parts - 1) / a.parts;
+    a.per = (a.E + nthr - 1) / nthr;
+    a.nact = ((a.E + a.per - 1) / a.per + 31) & ~31;
+    const int ncol = (a.parts * a.cols + 31) & ~31;
+    a.nwork = ncol > a.nact ? ncol : a.nact;
+    return a;
+}
+
+// Padded size of an expert block of c rows.
+__device__ __forceinline__ int padded(int c, int align)
+{
+    return align == 1 ? c : (c + align - 1) / align * align;
+}
+
 // The last CTA of a layout-producing grid to finish computes, alone, the
-// column prefix over tiles, the per-expert counts and the offsets.  Every CTA
-// calls this after writing its tile words and per-tile counts; only the CTA
-// that arrives last does the work.  No CTA waits on another: the counter only
-// tells the CTA that arrives last that all tiles are written.
-// The one-byte counts are stored expert-major, tile_cnt[e][tile], so a
-// thread reads its run of tiles of one expert in 16-byte vectors, all in
-// flight at once; global memory is read once and written once, and
-// everything in between stays in shared memory.
+// group bases (column prefix over groups of 16 tiles), the per-expert counts
+// and the offsets.  Every CTA calls this after writing its tile words and
+// per-tile counts; only the CTA that arrives last does the work.  No CTA waits
+// on another: the counter only tells the CTA that arrives last that all tiles
+// are written.
+// The group vectors of consecutive experts are adjacent, so a warp's loads
+// are contiguous; each thread keeps up to kTailVec groups in flight.  Only
+// the first nwork threads (whole warps) go on: every warp of a 1024-thread
+// CTA running the tail would cost 32 warps' issue slots per instruction of a
+// serial chain.
 __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* smem)
 {
     // The barrier orders every thread's tile writes before thread 0's
-    // GPU-scope fence, which orders them before the arrival count (one fence
-    // per CTA: a fence in every thread costs microseconds).
+    // arrival, an atomic add with release semantics at GPU scope; its acquire
+    // side, with the barrier after it, orders the last CTA's reads after every
+    // other CTA's writes.
     __shared__ int s_last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(a.done, 1u);
-        __threadfence();
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(a.done)
+                     : "memory");
         s_last = (prev == gridDim.x - 1) ? 1 : 0;
     }
     __syncthreads();
-    if (!s_last) return;
+    const int tid = threadIdx.x, nwork = a.nwork;
+    if (!s_last || tid >= nwork) return;
 
-    const int nthr = blockDim.x, tid = threadIdx.x;
     const int E = a.E, ntiles = a.ntiles;
-    int* s_part = smem;                 // [nthr]
-    int* s_warp = smem + nthr;          // [32]
+    const int ngroups = (ntiles + kGroupTiles - 1) / kGroupTiles;
+    int* s_part = smem;                 // [nwork]
+    int* s_warp = smem + 1024;          // [32]
     int* s_cnt = s_warp + 32;           // [E]
-    int* s_off = s_cnt + kMaxExperts;   // [E + 1]
+    int* s_off = s_cnt + kMaxExperts;   // [E]
 
-    // tpc threads share one expert column, each taking a run of rp tiles
-    // (a multiple of 16: whole vectors)
-    constexpr int kVec = 8;  // 16-byte vectors held in registers (128 tiles)
-    int tpc = 1;
-    while (tpc * 2 * E <= nthr) tpc *= 2;
-    const int cols_per_pass = nthr / tpc;
-    const int col_in = tid % cols_per_pass, part = tid / cols_per_pass;
-    const int rp = (((ntiles + tpc - 1) / tpc) + 15) & ~15;
-    const int r0 = min(part * rp, ntiles), r1 = min(r0 + rp, ntiles);
-    const int nv = (r1 - r0 + 15) / 16;
-    for (int c0 = 0; c0 < E; c0 += cols_per_pass) {
+    // Column pass: `parts` runs of rg consecutive groups per column; thread
+    // (part, col) = (tid / cols, tid % cols).
+    const int cols = a.cols, parts = a.parts, rg = a.rg;
+    const int part = tid / cols, col_in = tid - part * cols;
+    const int g0 = min(part * rg, ngroups), g1 = min(g0 + rg, ngroups);
+    const uint4* vec = reinterpret_cast<const uint4*>(a.tile_cnt);
+    for (int c0 = 0; c0 < E; c0 += cols) {
         const int col = c0 + col_in;
-        const bool act = col < E;
-        const uint8_t* src = a.tile_cnt + (size_t)col * a.cnt_stride + r0;
-        uint4 v[kVec];
+        const bool act = part < parts && col < E;
+        int gs[kTailVec];
         int sum = 0;
         if (act) {
-            for (int b0 = 0; b0 < nv; b0 += kVec) {
+            for (int b = g0; b < g1; b += kTailVec) {
+                uint4 v[kTailVec];
 #pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                    v[i] = (b0 + i < nv) ? __ldcg(reinterpret_cast<const uint4*>(src) + b0 + i)
-                                         : make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < kTailVec; ++i)
+                    v[i] = (b + i < g1) ? __ldcg(vec + (size_t)(b + i) * E + col)
+                                        : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) {
-                    const int t0 = r0 + 16 * (b0 + i);
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int lim = r1 - (t0 + 4 * q);  // bytes of this word that count
-                        const uint32_t m = lim >= 4 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << (8 * lim)) - 1u);
-                        sum += byte_sum(w[q] & m);
-                    }
+                for (int i = 0; i < kTailVec; ++i) {
+                    gs[i] = vec_byte_sum(v[i], ntiles - (b + i) * kGroupTiles);
+                    sum += gs[i];
                 }
             }
         }
-        s_part[tid] = sum;
-        __syncthreads();
-        if (act) {
-            int run = 0, total = 0;
-            for (int q = 0; q < tpc; ++q) {
-                const int x = s_part[q * cols_per_pass + col_in];
-                if (q < part) run += x;
+        int run = 0, total = sum;
+        if (parts > 1) {
+            s_part[tid] = sum;
+            asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
+            total = 0;
+            for (int q = 0; q < parts; ++q) {
+                const int x = s_part[q * cols + col_in];
+                run += q < part ? x : 0;
                 total += x;
             }
-            for (int b0 = 0; b0 < nv; b0 += kVec) {
-                if (nv > kVec) {  // runs longer than the registers hold: read again
+        }
+        if (act) {
+            for (int b = g0; b < g1; b += kTailVec) {
+                if (g1 - g0 > kTailVec) {  // runs longer than the registers hold: read again
+                    uint4 v[kTailVec];
 #pragma unroll
-                    for (int i = 0; i < kVec; ++i)
-                        v[i] = (b0 + i < nv) ? __ldcg(reinterpret_cast<const uint4*>(src) + b0 + i)
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                    for (int i = 0; i < kTailVec; ++i)
+                        v[i] = (b + i < g1) ? __ldcg(vec + (size_t)(b + i) * E + col)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int i = 0; i < kTailVec; ++i)
+                        gs[i] = vec_byte_sum(v[i], ntiles - (b + i) * kGroupTiles);
                 }
-                const int nvb = min(kVec, nv - b0);
 #pragma unroll
-                for (int i = 0; i < kVec; ++i) {
-                    if (i >= nvb) break;  // only the vectors that hold tiles
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                    const int t0 = r0 + 16 * (b0 + i);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        if (t0 + q < r1) {
-                            a.tile_base[(size_t)(t0 + q) * E + col] = run;
-                            run += (int)((w[q >> 2] >> (8 * (q & 3))) & 0xffu);
-                        }
+                for (int i = 0; i < kTailVec; ++i) {
+                    if (b + i < g1) {
+                        a.grp_base[(size_t)(b + i) * E + col] = run;
+                        run += gs[i];
                     }
                 }
             }
             if (part == 0) s_cnt[col] = total;
         }
-        __syncthreads();
+        if (parts > 1) asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
     }
+    asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
 
-    // exclusive prefix of the (padded) counts over experts (shared memory only)
-    const int al = a.align;
-    const int per = (E + nthr - 1) / nthr;
+    // Prefix of the padded counts over experts: `per` consecutive experts per
+    // thread, on the first nact threads (whole warps).
+    const int per = a.per, nact = a.nact;
+    const int al = a.align, L = a.L;
     const int lo = min(tid * per, E), hi = min(lo + per, E);
-    int sum = 0;
-    for (int e = lo; e < hi; ++e) sum += (s_cnt[e] + al - 1) / al * al;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int x = lane < nwarps ? s_warp[lane] : 0;
+    const bool pre = tid < nact;
+    int sum = 0, incl = 0;
+    const int lane = tid & 31, warp = tid >> 5;
+    if (pre) {
+        for (int e = lo; e < hi; ++e) sum += padded(s_cnt[e], al);
+        incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += n;
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
         }
-        if (lane < nwarps) s_warp[lane] = x;
+        if (lane == 31) s_warp[warp] = incl;
     }
-    __syncthreads();
-    int run = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);
-    for (int e = lo; e < hi; ++e) {
-        s_off[e] = run;
-        run += (s_cnt[e] + al - 1) / al * al;
+    asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
+    int32_t* const host = a.host_out;
+    if (pre) {
+        int run = incl - sum;
+        for (int w = 0; w < warp; ++w) run += s_warp[w];
+        for (int e = lo; e < hi; ++e) {
+            const int c = s_cnt[e];
+            a.cnt[e] = c;
+            a.off[e] = run;
+            s_off[e] = run;
+            if (host) {
+                host[e] = run;
+                host[E + 1 + a.R + e] = c;
+            }
+            run += padded(c, al);
+        }
+        if (lo < E && hi == E) {  // the thread holding the last expert: the totals
+            a.off[E] = run;
+            a.roff[a.R] = run;
+            if (host) host[E] = run;
+        }
     }
-    if (tid == nthr - 1) s_off[E] = s_warp[nwarps - 1];
-    __syncthreads();
-    for (int e = tid; e < E; e += nthr) {
-        a.cnt[e] = s_cnt[e];
-        a.off[e] = s_off[e];
-    }
-    if (tid == 0) a.off[E] = s_off[E];
-    const int L = E / a.R;
-    for (int r = tid; r < a.R; r += nthr) {
+    if (tid == 0) *a.done = 0u;  // ready for the next launch on this handle
+    asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
+    for (int r = tid; r < a.R; r += nwork) {
         int c = 0;
         for (int l = 0; l < L; ++l) c += s_cnt[r * L + l];
-        a.roff[r] = s_off[r * L];
         a.rcnt[r] = c;
-        if (a.host_out) a.host_out[E + 1 + r] = c;
+        a.roff[r] = s_off[r * L];
+        if (host) host[E + 1 + r] = c;
     }
-    if (tid == 0) {
-        a.roff[a.R] = s_off[E];
-        *a.done = 0u;  // ready for the next launch on this handle
-    }
-    if (a.host_out) {
+    if (host) {
         // the host's copy of the counts (one host synchronisation of HT mode
         // waits for these words, not for the rest of the stream)
-        for (int e = tid; e <= E; e += nthr) a.host_out[e] = s_off[e];
-        for (int e = tid; e < E; e += nthr) a.host_out[E + 1 + a.R + e] = s_cnt[e];
-        __syncthreads();
+        asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory");
         if (tid == 0) {
             __threadfence_system();
-            reinterpret_cast<volatile unsigned*>(a.host_out)[E + 1 + a.R + E] = a.seq;
+            reinterpret_cast<volatile unsigned*>(host)[E + 1 + a.R + E] = a.seq;
         }
     }
 }
@@ -202,8 +265,9 @@ __device__ __forceinline__ int token_pair_row(const RowArgs& a, int t, int lane)
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const bool dup = (peers & ((1u << lane) - 1u)) != 0u;
     if (lane >= a.k || e < 0 || e >= a.E || dup) return -1;
-    const size_t q = (size_t)(t >> 5) * a.E + e;
-    const int rank = __ldg(a.tile_base + q) + __popc(__ldg(a.tile_word + q) & ((1u << (t & 31)) - 1u));
+    const int tile = t / kTileTokens;
+    const int rank = pairs_before_tile(a.tile_cnt, a.grp_base, a.E, e, tile) +
+                     __popc(__ldg(a.tile_word + (size_t)tile * a.E + e) & ((1u << (t & 31)) - 1u));
     return (a.mode == MOE_EP_HT) ? __ldg(a.off + e) + rank : e * a.S + rank;
 }
 

@@ -86,13 +86,14 @@ __global__ void __launch_bounds__(kThreads) node_bits_kernel(NodeArgs a, LayoutA
     for (int n = tid; n < a.N; n += blockDim.x) {
         const uint32_t wd = s_word[n];
         la.tile_word[(size_t)blockIdx.x * a.N + n] = wd;
-        la.tile_cnt[(size_t)n * la.cnt_stride + blockIdx.x] = (uint8_t)__popc(wd);
+        la.tile_cnt[tile_cnt_index(blockIdx.x, n, a.N)] = (uint8_t)__popc(wd);
     }
     finish_layout_if_last(la, s_scratch);
 }
 
 __global__ void __launch_bounds__(kThreads) node_rows_kernel(NodeArgs a, const uint32_t* tile_word,
-                                                             const int32_t* tile_base,
+                                                             const uint8_t* tile_cnt,
+                                                             const int32_t* grp_base,
                                                              const int32_t* node_off,
                                                              int32_t* node_src, uint32_t* node_mask)
 {
@@ -100,9 +101,10 @@ __global__ void __launch_bounds__(kThreads) node_rows_kernel(NodeArgs a, const u
     for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpc) {
         const TokenNodes r = token_nodes(a, t, lane);
         if (!r.node_leader) continue;
-        const size_t q = (size_t)(t >> 5) * a.N + r.node;
-        const int row = __ldg(node_off + r.node) + __ldg(tile_base + q) +
-                        __popc(__ldg(tile_word + q) & ((1u << (t & 31)) - 1u));
+        const int tile = t / kTileTokens;
+        const int row = __ldg(node_off + r.node) +
+                        pairs_before_tile(tile_cnt, grp_base, a.N, r.node, tile) +
+                        __popc(__ldg(tile_word + (size_t)tile * a.N + r.node) & ((1u << (t & 31)) - 1u));
         node_src[row] = t;
         node_mask[row] = r.mask;
     }
@@ -114,13 +116,13 @@ cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned
                                int32_t* node_src, uint32_t* node_mask, int sm_count, cudaStream_t s)
 {
     if (a.T <= 0) return cudaSuccess;
-    node_bits_kernel<<<la.ntiles, kThreads, 0, s>>>(a, la, stats);
+    node_bits_kernel<<<la.ntiles, kThreads, 0, s>>>(a, tail_planned(la, kThreads), stats);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     int blocks = (a.T + 7) / 8;
     if (blocks > sm_count * 8) blocks = sm_count * 8;
-    node_rows_kernel<<<blocks, kThreads, 0, s>>>(a, la.tile_word, la.tile_base, la.off, node_src,
-                                                 node_mask);
+    node_rows_kernel<<<blocks, kThreads, 0, s>>>(a, la.tile_word, la.tile_cnt, la.grp_base, la.off,
+                                                 node_src, node_mask);
     return cudaGetLastError();
 }
 

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
     for (int e = tid; e < p.E; e += blockDim.x) {
         const uint32_t wd = s_word[e];
         la.tile_word[(size_t)tile * p.E + e] = wd;
-        la.tile_cnt[(size_t)e * la.cnt_stride + tile] = (uint8_t)__popc(wd);
+        la.tile_cnt[tile_cnt_index(tile, e, p.E)] = (uint8_t)__popc(wd);
     }
     finish_layout_if_last(la, s_scratch);
 }
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
     for (int e = tid; e < E; e += blockDim.x) {
         const uint32_t wd = s_word[e];
         la.tile_word[(size_t)tile * E + e] = wd;
-        la.tile_cnt[(size_t)e * la.cnt_stride + tile] = (uint8_t)__popc(wd);
+        la.tile_cnt[tile_cnt_index(tile, e, E)] = (uint8_t)__popc(wd);
     }
     finish_layout_if_last(la, s_scratch);
 }
@@ -313,11 +313,12 @@ void launch_route_mg(const float* scores, int T, const RouteParams& p, int32_t* 
                      int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+    const LayoutArgs lt = tail_planned(la, 1024);
     // the group list holds MG >= m keys (m = 1, 2: two; 3, 4: four)
     if (!p.limit || p.m <= 2)
-        route_kernel<EPL, VEC, 2><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, la);
+        route_kernel<EPL, VEC, 2><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, lt);
     else
-        route_kernel<EPL, VEC, 4><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, la);
+        route_kernel<EPL, VEC, 4><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, lt);
 }
 
 template <int EPL>
@@ -354,7 +355,7 @@ cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* i
 {
     if (T <= 0) return cudaSuccess;
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
-    layout_bits_kernel<<<ntiles, 256, 0, s>>>(topk_idx, T, k, idx_copy, la, err);
+    layout_bits_kernel<<<ntiles, 256, 0, s>>>(topk_idx, T, k, idx_copy, tail_planned(la, 256), err);
     return cudaGetLastError();
 }
 

@@ -26,10 +26,11 @@ namespace {
 // (for example T = 8192 tokens with E = 256 experts).
 constexpr int kStaticCells = 65536;
 constexpr size_t kWordBytes = sizeof(uint32_t) * kStaticCells;               // tile words
-constexpr size_t kBaseBytes = sizeof(int32_t) * kStaticCells;                // column prefix
-constexpr size_t kCntBytes = (size_t)kStaticCells + 16 * (size_t)kMaxExperts; // byte counts, padded rows
+// group bases: ceil(ntiles / 16) * E <= kStaticCells / 16 + E
+constexpr size_t kBaseBytes = sizeof(int32_t) * (kStaticCells / 16 + kMaxExperts);
+constexpr size_t kCntBytes = (size_t)kStaticCells + 16 * (size_t)kMaxExperts; // byte counts, last group padded
 constexpr size_t kDoneBytes = 256;                                           // arrival counter
-constexpr size_t kScratchBytes = kWordBytes + kBaseBytes + kCntBytes + kDoneBytes;  // 592 KiB
+constexpr size_t kScratchBytes = kWordBytes + kBaseBytes + kCntBytes + kDoneBytes;  // 346.25 KiB
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
@@ -110,7 +111,7 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
 
     LayoutArgs la;
     la.tile_word = reinterpret_cast<uint32_t*>(base);
-    la.tile_base = reinterpret_cast<int32_t*>(base + kWordBytes);
+    la.grp_base = reinterpret_cast<int32_t*>(base + kWordBytes);
     la.tile_cnt = base + kWordBytes + kBaseBytes;
     la.done = reinterpret_cast<unsigned*>(base + kWordBytes + kBaseBytes + kCntBytes);
     la.cnt = cnt;
@@ -120,7 +121,6 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     la.E = experts;
     la.R = ranks;
     la.ntiles = ntiles;
-    la.cnt_stride = (ntiles + 15) & ~15;
     la.host_out = nullptr;
     la.seq = 0u;
     la.align = 1;
@@ -140,7 +140,8 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     RowArgs ra;
     ra.idx = topk_idx;
     ra.tile_word = la.tile_word;
-    ra.tile_base = la.tile_base;
+    ra.tile_cnt = la.tile_cnt;
+    ra.grp_base = la.grp_base;
     ra.off = off;
     ra.T = T;
     ra.k = k;

@@ -266,7 +266,7 @@ MOE_EP_API int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off,
  * handle of the same mode, experts, ranks and slots, with the same options:
  * topk_idx [T][k], topk_w [T][k] (may be NULL), row [T][k], cnt [E],
  * off [E+1], rcnt [R], roff [R+1], all device buffers owned by the caller.
- * The layout's scratch lives in one static device array of 592 KiB that every
+ * The layout's scratch lives in one static device array of 346.25 KiB that every
  * GPU loading the library holds until exit; it is never allocated or freed.
  * Capacity: ceil(num_tokens / 32) * experts <= 65536 (e.g. 8192 tokens with
  * 256 experts); larger sizes return MOE_EP_ERR_OVERFLOW without launching.
