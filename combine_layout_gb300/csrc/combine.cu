@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
     const uint4* __restrict__ y, int T, int k, int nvec, const int32_t* __restrict__ row,
     const float* __restrict__ w, uint4* __restrict__ out)
 {
+    griddep_wait();
     __shared__ int s_row[KMAX];
     __shared__ float s_w[KMAX];
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -97,18 +98,22 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
     const uint4* yy = (const uint4*)y;
     uint4* oo = (uint4*)out;
     if (k <= 1)
-        combine_kernel<1><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    else if (k <= 2)
-        combine_kernel<2><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    else if (k <= 4)
-        combine_kernel<4><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    else if (k <= 8)
-        combine_kernel<8><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    else if (k <= 16)
-        combine_kernel<16><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    else
-        combine_kernel<32><<<blocks, kThreads, 0, s>>>(yy, T, k, nvec, row, w, oo);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<1>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
+                          row, w, oo);
+    if (k <= 2)
+        return launch_pdl(combine_kernel<2>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
+                          row, w, oo);
+    if (k <= 4)
+        return launch_pdl(combine_kernel<4>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
+                          row, w, oo);
+    if (k <= 8)
+        return launch_pdl(combine_kernel<8>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
+                          row, w, oo);
+    if (k <= 16)
+        return launch_pdl(combine_kernel<16>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
+                          row, w, oo);
+    return launch_pdl(combine_kernel<32>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec, row, w,
+                      oo);
 }
 
 }  // namespace moeep

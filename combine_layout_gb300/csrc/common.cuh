@@ -22,6 +22,39 @@ constexpr int kErrSlots = 4;
 constexpr int kErrRange = 0;
 constexpr int kErrDuplicate = 1;
 
+// Every kernel of the library is launched with programmatic stream
+// serialization: its CTAs may become resident while the kernel before it on
+// the stream is still finishing (launch latency and that kernel's tail
+// overlap), and each kernel executes griddep_wait() before its first global
+// memory access, which returns once the kernels before it have completed and
+// their writes are visible.  Kernels that produce a layout signal their
+// dependents as soon as every CTA has written its tile (the grid's last CTA
+// then finishes the layout while the next kernel's CTAs are being placed).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
 struct RouteParams {
     int E;      // experts
     int G;      // routing groups (nodes)

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
                                                            const float* __restrict__ scale,
                                                            uint4* __restrict__ y)
 {
+    griddep_wait();
     __shared__ int s_pre[kMaxExperts + 1];
     __shared__ int s_part[kThreads];
     // exclusive prefix of the actual counts
@@ -116,9 +117,8 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
                            const uint8_t* q, const float* scale, void* y, int sm_count,
                            cudaStream_t s)
 {
-    dequant_kernel<<<sm_count * 8, kThreads, 0, s>>>(cnt, off, E, S, mode, H, (const uint4*)q, scale,
-                                                    (uint4*)y);
-    return cudaGetLastError();
+    return launch_pdl(dequant_kernel, dim3(sm_count * 8), dim3(kThreads), s, cnt, off, E, S, mode, H,
+                      (const uint4*)q, scale, (uint4*)y);
 }
 
 }  // namespace moeep

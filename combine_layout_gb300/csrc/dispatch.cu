@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
     int32_t* __restrict__ recv_cnt)
 {
+    griddep_wait();
     __shared__ int s_row[kMaxTopk];
     if (blockIdx.x == 0 && recv_cnt)
         for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
     const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
 {
+    griddep_wait();
     __shared__ int s_row[kMaxTopk];
     if (blockIdx.x == 0 && recv_cnt)
         for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
@@ -184,13 +186,11 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
     const int nvec = H / 8;
     const int blocks = ra.T < 1 ? 1 : ra.T;
     if (fp8)
-        dispatch_fp8_kernel<<<blocks, kThreads, 0, s>>>(ra, (const uint4*)x, nvec, row,
-                                                        (uint2*)recv_x, recv_scale, recv_src, cnt,
-                                                        recv_cnt);
-    else
-        dispatch_bf16_kernel<<<blocks, kThreads, 0, s>>>(ra, (const uint4*)x, nvec, row,
-                                                         (uint4*)recv_x, recv_src, cnt, recv_cnt);
-    return cudaGetLastError();
+        return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
+                          (const uint4*)x, nvec, row, (uint2*)recv_x, recv_scale, recv_src, cnt,
+                          recv_cnt);
+    return launch_pdl(dispatch_bf16_kernel, dim3(blocks), dim3(kThreads), s, ra, (const uint4*)x,
+                      nvec, row, (uint4*)recv_x, recv_src, cnt, recv_cnt);
 }
 
 }  // namespace moeep

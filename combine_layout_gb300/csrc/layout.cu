@@ -8,6 +8,7 @@ namespace {
 
 __global__ void __launch_bounds__(256) rowmap_kernel(RowArgs a, int32_t* __restrict__ row)
 {
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
     for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpc) {
@@ -23,8 +24,7 @@ cudaError_t launch_rowmap(const RowArgs& ra, int32_t* row, int sm_count, cudaStr
     if (ra.T <= 0) return cudaSuccess;
     int blocks = (ra.T + 7) / 8;
     if (blocks > sm_count * 8) blocks = sm_count * 8;
-    rowmap_kernel<<<blocks, 256, 0, s>>>(ra, row);
-    return cudaGetLastError();
+    return launch_pdl(rowmap_kernel, dim3(blocks), dim3(256), s, ra, row);
 }
 
 }  // namespace moeep

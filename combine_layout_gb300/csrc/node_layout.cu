@@ -59,6 +59,7 @@ __device__ __forceinline__ TokenNodes token_nodes(const NodeArgs& a, int t, int 
 __global__ void __launch_bounds__(kThreads) node_bits_kernel(NodeArgs a, LayoutArgs la,
                                                              unsigned long long* stats)
 {
+    griddep_wait();
     __shared__ uint32_t s_word[kMaxExperts];
     __shared__ int s_scratch[kTailSmemInts];
     __shared__ unsigned long long s_stats[4];
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) node_bits_kernel(NodeArgs a, LayoutA
         la.tile_word[(size_t)blockIdx.x * a.N + n] = wd;
         la.tile_cnt[tile_cnt_index(blockIdx.x, n, a.N)] = (uint8_t)__popc(wd);
     }
+    griddep_launch_dependents();
     finish_layout_if_last(la, s_scratch);
 }
 
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kThreads) node_rows_kernel(NodeArgs a, const u
                                                              const int32_t* node_off,
                                                              int32_t* node_src, uint32_t* node_mask)
 {
+    griddep_wait();
     const int lane = threadIdx.x & 31, wpc = blockDim.x >> 5;
     for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpc) {
         const TokenNodes r = token_nodes(a, t, lane);
@@ -116,14 +119,14 @@ cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned
                                int32_t* node_src, uint32_t* node_mask, int sm_count, cudaStream_t s)
 {
     if (a.T <= 0) return cudaSuccess;
-    node_bits_kernel<<<la.ntiles, kThreads, 0, s>>>(a, tail_planned(la, kThreads), stats);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(node_bits_kernel, dim3(la.ntiles), dim3(kThreads), s, a,
+                               tail_planned(la, kThreads), stats);
     if (e != cudaSuccess) return e;
     int blocks = (a.T + 7) / 8;
     if (blocks > sm_count * 8) blocks = sm_count * 8;
-    node_rows_kernel<<<blocks, kThreads, 0, s>>>(a, la.tile_word, la.tile_cnt, la.grp_base, la.off,
-                                                 node_src, node_mask);
-    return cudaGetLastError();
+    return launch_pdl(node_rows_kernel, dim3(blocks), dim3(kThreads), s, a,
+                      (const uint32_t*)la.tile_word, (const uint8_t*)la.tile_cnt,
+                      (const int32_t*)la.grp_base, (const int32_t*)la.off, node_src, node_mask);
 }
 
 }  // namespace moeep

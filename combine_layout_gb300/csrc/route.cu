@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
                                                      int32_t* __restrict__ idx_copy,
                                                      float* __restrict__ topk_w, LayoutArgs la)
 {
+    griddep_wait();
     __shared__ uint32_t s_word[kMaxExperts];
     __shared__ int s_scratch[kTailSmemInts];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
         la.tile_word[(size_t)tile * p.E + e] = wd;
         la.tile_cnt[tile_cnt_index(tile, e, p.E)] = (uint8_t)__popc(wd);
     }
+    griddep_launch_dependents();
     finish_layout_if_last(la, s_scratch);
 }
 
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ idx_copy,
                                                           LayoutArgs la, volatile unsigned* err)
 {
+    griddep_wait();
     __shared__ uint32_t s_word[kMaxExperts];
     __shared__ int s_scratch[kTailSmemInts];
     const int tid = threadIdx.x, E = la.E;
@@ -305,30 +308,32 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
         la.tile_word[(size_t)tile * E + e] = wd;
         la.tile_cnt[tile_cnt_index(tile, e, E)] = (uint8_t)__popc(wd);
     }
+    griddep_launch_dependents();
     finish_layout_if_last(la, s_scratch);
 }
 
 template <int EPL, bool VEC>
-void launch_route_mg(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
+cudaError_t launch_route_mg(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
                      int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
     const LayoutArgs lt = tail_planned(la, 1024);
     // the group list holds MG >= m keys (m = 1, 2: two; 3, 4: four)
     if (!p.limit || p.m <= 2)
-        route_kernel<EPL, VEC, 2><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, lt);
-    else
-        route_kernel<EPL, VEC, 4><<<ntiles, 1024, 0, s>>>(scores, T, p, topk_idx, idx_copy, topk_w, lt);
+        return launch_pdl(route_kernel<EPL, VEC, 2>, dim3(ntiles), dim3(1024), s, scores, T, p,
+                          topk_idx, idx_copy, topk_w, lt);
+    return launch_pdl(route_kernel<EPL, VEC, 4>, dim3(ntiles), dim3(1024), s, scores, T, p,
+                      topk_idx, idx_copy, topk_w, lt);
 }
 
 template <int EPL>
-void launch_route_epl(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
-                      int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
+cudaError_t launch_route_epl(const float* scores, int T, const RouteParams& p, int32_t* topk_idx,
+                             int32_t* idx_copy, float* topk_w, const LayoutArgs& la,
+                             cudaStream_t s)
 {
     if (EPL >= 4 && p.vec4)
-        launch_route_mg<EPL, (EPL >= 4)>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    else
-        launch_route_mg<EPL, false>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+        return launch_route_mg<EPL, (EPL >= 4)>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+    return launch_route_mg<EPL, false>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
 }
 
 }  // namespace
@@ -337,17 +342,11 @@ cudaError_t launch_route(const float* scores, int T, const RouteParams& p, int32
                          int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     if (T <= 0) return cudaSuccess;
-    if (p.epl <= 1)
-        launch_route_epl<1>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    else if (p.epl <= 2)
-        launch_route_epl<2>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    else if (p.epl <= 4)
-        launch_route_epl<4>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    else if (p.epl <= 8)
-        launch_route_epl<8>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    else
-        launch_route_epl<16>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
-    return cudaGetLastError();
+    if (p.epl <= 1) return launch_route_epl<1>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+    if (p.epl <= 2) return launch_route_epl<2>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+    if (p.epl <= 4) return launch_route_epl<4>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+    if (p.epl <= 8) return launch_route_epl<8>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
+    return launch_route_epl<16>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
 }
 
 cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* idx_copy,
@@ -355,8 +354,8 @@ cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* i
 {
     if (T <= 0) return cudaSuccess;
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
-    layout_bits_kernel<<<ntiles, 256, 0, s>>>(topk_idx, T, k, idx_copy, tail_planned(la, 256), err);
-    return cudaGetLastError();
+    return launch_pdl(layout_bits_kernel, dim3(ntiles), dim3(256), s, topk_idx, T, k, idx_copy,
+                      tail_planned(la, 256), err);
 }
 
 }  // namespace moeep
