@@ -16,6 +16,8 @@ Each wrapper follows a passage of the source pages (cited in moe_oracle.c):
               state and reduce to token order); "高吞吐模式" (BF16 weighted sum)
   node_layout -- "高吞吐模式": one copy per remote node (same-position GPU), then
               forwarding to the GPUs holding the experts; the routing statistics
+  rank_layout / expand / combine_dedup -- "高吞吐模式" routing simulation, "按目标卡去重"
+              (one copy per destination GPU), and BF16 weighted sums sent back
 """
 from __future__ import annotations
 
@@ -75,8 +77,12 @@ def _load():
     lib.orc_dispatch.argtypes = [P, i64, i32, i32, P, i64, i32, P, P, P]
     lib.orc_node_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
     lib.orc_combine.argtypes = [P, i64, i32, P, P, i64, i32, P, i64, P]
+    lib.orc_rank_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
+    lib.orc_expand.argtypes = [P, P, i64, i64, i32, P, P, P, i32, i32, P, P, i64, i32, i64, P, P, P]
+    lib.orc_combine_dedup.argtypes = [P, i64, i32, P, P, P, i64, i32, i32, i32, P, i64, P, i64, P, P]
     for f in ("orc_quant_row", "orc_route", "orc_layout", "orc_dispatch", "orc_combine",
-              "orc_node_layout", "orc_layout_aligned", "orc_dequant_rows"):
+              "orc_node_layout", "orc_layout_aligned", "orc_dequant_rows", "orc_rank_layout",
+              "orc_expand", "orc_combine_dedup"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -231,3 +237,68 @@ def combine(y_bf16_bits, row, w, tokens=None) -> np.ndarray:
     if st != OK:
         raise ValueError(f"orc_combine status {st}")
     return out
+
+
+def rank_layout(topk_idx, experts: int, ranks: int):
+    """Per-rank dedup layout.  Returns (dict(cnt, off, drow, src, mask), status)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    cnt = np.empty(ranks, np.int32)
+    off = np.empty(ranks + 1, np.int32)
+    drow = np.empty((T, k), np.int32)
+    cap = max(T * min(k, ranks), 1)
+    src = np.full(cap, -1, np.int32)
+    mask = np.zeros(cap, np.uint32)
+    st = _load().orc_rank_layout(_p(idx), T, k, experts, ranks, _p(cnt), _p(off), _p(drow),
+                                 _p(src), _p(mask))
+    if st == ERR_INVALID and (experts % ranks or experts // ranks > 32):
+        raise ValueError("orc_rank_layout: bad shape")
+    n = int(off[-1])
+    return dict(cnt=cnt, off=off, drow=drow, src=src[:n], mask=mask[:n]), st
+
+
+def expand(dx, dscale, dsrc, dmask, rank_off, experts: int, topk_idx, row, nrows: int):
+    """Receiver-side expansion of dedup rows (bf16 [nd][H] or e4m3 [nd][H] with
+    dscale [nd][H/128]) into the expert-major rows.  Returns (recv_x, recv_scale, recv_src)."""
+    dx = np.ascontiguousarray(dx)
+    nd = dx.shape[0]
+    row_bytes = dx.shape[1] * dx.itemsize
+    fp8 = dscale is not None
+    nscale = dscale.shape[1] if fp8 else 0
+    recv_x = np.zeros((nrows,) + dx.shape[1:], dx.dtype)
+    recv_scale = np.zeros((nrows, max(nscale, 1)), np.float32)
+    recv_src = np.full(nrows, -1, np.int32)
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    R = len(rank_off) - 1
+    st = _load().orc_expand(_p(dx), _p(_c(dscale, np.float32)) if fp8 else None, nd, row_bytes,
+                            nscale, _p(_c(dsrc, np.int32)), _p(_c(dmask, np.uint32)),
+                            _p(_c(rank_off, np.int32)), R, experts, _p(idx), _p(_c(row, np.int32)),
+                            T, k, nrows, _p(recv_x), _p(recv_scale), _p(recv_src))
+    if st != OK:
+        raise ValueError(f"orc_expand status {st}")
+    return recv_x, (recv_scale if fp8 else None), recv_src
+
+
+def combine_dedup(y_bf16_bits, topk_idx, row, w, experts: int, ranks: int, drow, nd: int,
+                  tokens=None, want_partial: bool = False):
+    """Two-stage combine over dedup rows.  Returns out [T or len(tokens), H]
+    (and the partial rows [nd][H] when want_partial)."""
+    y = _c(y_bf16_bits, np.uint16)
+    nrows, H = y.shape
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    if tokens is None:
+        tk, ntok, n = None, 0, T
+    else:
+        tk = _c(tokens, np.int64).reshape(-1)
+        ntok = n = tk.size
+    out = np.empty((n, H), np.uint16)
+    partial = np.zeros((max(nd, 1), H), np.uint16) if want_partial else None
+    st = _load().orc_combine_dedup(_p(y), nrows, H, _p(idx), _p(_c(row, np.int32)),
+                                   _p(_c(w, np.float32)), T, k, experts, ranks,
+                                   _p(_c(drow, np.int32)), nd, None if tk is None else _p(tk),
+                                   ntok, None if partial is None else _p(partial), _p(out))
+    if st != OK:
+        raise ValueError(f"orc_combine_dedup status {st}")
+    return (out, partial[:nd]) if want_partial else out

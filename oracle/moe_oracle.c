@@ -453,3 +453,130 @@ int orc_combine(const uint16_t* y, int64_t nrows, int H, const int32_t* row, con
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------- */
+/* per-rank dedup layout, expansion and two-stage combine                     */
+/* ------------------------------------------------------------------------- */
+
+int orc_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int32_t* rank_cnt,
+                    int32_t* rank_off, int32_t* drow, int32_t* dsrc, uint32_t* dmask)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0 || E / R > 32) return ORC_ERR_INVALID;
+    const int L = E / R;
+    int status = ORC_OK;
+    uint32_t* m = (uint32_t*)calloc((size_t)R, sizeof(uint32_t));
+    for (int r = 0; r < R; ++r) rank_cnt[r] = 0;
+    /* pass 1: ranks each token needs */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int r = 0; r < R; ++r) m[r] = 0;
+        for (int j = 0; j < k; ++j) {
+            int kind = pair_kind(topk_idx + t * k, j, E);
+            if (kind < 0) status = ORC_ERR_INVALID;
+            if (kind != 1) continue;
+            int e = topk_idx[t * k + j];
+            m[e / L] |= 1u << (e % L);
+        }
+        for (int r = 0; r < R; ++r)
+            if (m[r]) rank_cnt[r] += 1;
+    }
+    rank_off[0] = 0;
+    for (int r = 0; r < R; ++r) rank_off[r + 1] = rank_off[r] + rank_cnt[r];
+    /* pass 2: rows rank-major, tokens ascending; the pair map names each
+     * token's row on a rank at the first valid pair on that rank */
+    int32_t* cursor = (int32_t*)calloc((size_t)R, sizeof(int32_t));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int r = 0; r < R; ++r) m[r] = 0;
+        for (int j = 0; j < k; ++j) {
+            if (pair_kind(topk_idx + t * k, j, E) != 1) continue;
+            int e = topk_idx[t * k + j];
+            m[e / L] |= 1u << (e % L);
+        }
+        for (int j = 0; j < k; ++j) drow[t * k + j] = -1;
+        for (int j = 0; j < k; ++j) {
+            if (pair_kind(topk_idx + t * k, j, E) != 1) continue;
+            int r = topk_idx[t * k + j] / L;
+            int first = 1;
+            for (int jj = 0; jj < j; ++jj)
+                if (pair_kind(topk_idx + t * k, jj, E) == 1 && topk_idx[t * k + jj] / L == r)
+                    first = 0;
+            if (!first) continue;
+            int q = rank_off[r] + cursor[r]++;
+            drow[t * k + j] = q;
+            dsrc[q] = (int32_t)t;
+            dmask[q] = m[r];
+        }
+    }
+    free(cursor);
+    free(m);
+    return status;
+}
+
+int orc_expand(const uint8_t* dx, const float* dscale, int64_t nd, int64_t row_bytes, int nscale,
+               const int32_t* dsrc, const uint32_t* dmask, const int32_t* rank_off, int R, int E,
+               const int32_t* topk_idx, const int32_t* row, int64_t T, int k, int64_t nrows,
+               uint8_t* recv_x, float* recv_scale, int32_t* recv_src)
+{
+    if (R < 1 || E % R != 0 || E / R > 32 || row_bytes < 1 || rank_off[R] > nd)
+        return ORC_ERR_INVALID;
+    const int L = E / R;
+    for (int r = 0; r < R; ++r)
+        for (int64_t q = rank_off[r]; q < rank_off[r + 1]; ++q) {
+            const int64_t t = dsrc[q];
+            if (t < 0 || t >= T) return ORC_ERR_INVALID;
+            for (int l = 0; l < L; ++l) {
+                if (!((dmask[q] >> l) & 1u)) continue;
+                const int e = r * L + l;
+                int64_t er = -1;
+                for (int j = 0; j < k && er < 0; ++j)
+                    if (pair_kind(topk_idx + t * k, j, E) == 1 && topk_idx[t * k + j] == e)
+                        er = row[t * k + j];
+                if (er < 0 || er >= nrows) return ORC_ERR_INVALID;
+                memcpy(recv_x + er * row_bytes, dx + q * row_bytes, (size_t)row_bytes);
+                if (dscale)
+                    memcpy(recv_scale + er * nscale, dscale + q * nscale, sizeof(float) * (size_t)nscale);
+                recv_src[er] = (int32_t)t;
+            }
+        }
+    return ORC_OK;
+}
+
+int orc_combine_dedup(const uint16_t* y, int64_t nrows, int H, const int32_t* topk_idx,
+                      const int32_t* row, const float* w, int64_t T, int k, int E, int R,
+                      const int32_t* drow, int64_t nd, const int64_t* tokens, int64_t ntok,
+                      uint16_t* partial, uint16_t* out)
+{
+    if (T < 0 || H <= 0 || k < 1 || R < 1 || E % R != 0) return ORC_ERR_INVALID;
+    const int L = E / R;
+    const int64_t n = tokens ? ntok : T;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    int status = ORC_OK;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) { status = ORC_ERR_INVALID; continue; }
+        for (int h = 0; h < H; ++h) acc[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int64_t q = drow[t * k + j];
+            if (q < 0) continue;              /* not the first pair of its rank */
+            if (q >= nd) { status = ORC_ERR_INVALID; continue; }
+            const int r = topk_idx[t * k + j] / L;
+            for (int h = 0; h < H; ++h) {
+                /* stage 1: this rank's weighted sum, rounded to bf16 once */
+                double p = 0.0;
+                for (int jj = 0; jj < k; ++jj) {
+                    if (pair_kind(topk_idx + t * k, jj, E) != 1) continue;
+                    if (topk_idx[t * k + jj] / L != r) continue;
+                    const int64_t er = row[t * k + jj];
+                    if (er < 0 || er >= nrows) { status = ORC_ERR_INVALID; continue; }
+                    p += (double)w[t * k + jj] * orc_bf16_to_double(y[er * H + h]);
+                }
+                const uint16_t pb = orc_bf16_from_double(p);
+                if (partial) partial[q * H + h] = pb;
+                /* stage 2: the source adds the ranks' partials */
+                acc[h] += orc_bf16_to_double(pb);
+            }
+        }
+        for (int h = 0; h < H; ++h) out[i * H + h] = orc_bf16_from_double(acc[h]);
+    }
+    free(acc);
+    return status;
+}

@@ -120,6 +120,42 @@ int orc_dispatch(const uint16_t* x, int64_t T, int H, int k, const int32_t* row,
 int orc_combine(const uint16_t* y, int64_t nrows, int H, const int32_t* row, const float* w,
                 int64_t T, int k, const int64_t* tokens, int64_t ntok, uint16_t* out);
 
+/* Per-rank dedup layout (HT): one row per (token, destination rank holding at
+ * least one of the token's experts) -- the page's "按目标卡去重" (dedup by
+ * destination GPU) in the routing simulation of "NVSHMEM 与 DeepEP：GPU 发起的通信",
+ * section "高吞吐模式": a token goes once to every rank that needs it.  Experts in
+ * contiguous blocks of L = E/R (rank = e / L), L <= 32.  Rows rank-major,
+ * tokens ascending.  Outputs: rank_cnt [R], rank_off [R+1], drow [T][k] = the
+ * row of pair (t, j) when j is the first valid pair of t on its rank, else -1;
+ * dsrc [rows] = token, dmask [rows] = bit l set when local expert l of the
+ * row's rank is one of the token's experts.  Invalid and repeated expert ids
+ * are skipped as in orc_layout (status ORC_ERR_INVALID when any is seen). */
+int orc_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int32_t* rank_cnt,
+                    int32_t* rank_off, int32_t* drow, int32_t* dsrc, uint32_t* dmask);
+
+/* Receiver-side expansion of dedup rows into the expert-major HT layout: every
+ * dedup row q of rank r (token t = dsrc[q]) is copied, payload bytes as they
+ * are (row_bytes per row; FP8 scales nscale floats per row when dscale is not
+ * NULL), to the expert rows of the local experts in dmask[q], ascending:
+ * expert e = r*L + l, row = row[t][j] for the pair (t, j) with topk_idx = e.
+ * recv_src of every written row gets t. */
+int orc_expand(const uint8_t* dx, const float* dscale, int64_t nd, int64_t row_bytes, int nscale,
+               const int32_t* dsrc, const uint32_t* dmask, const int32_t* rank_off, int R, int E,
+               const int32_t* topk_idx, const int32_t* row, int64_t T, int k, int64_t nrows,
+               uint8_t* recv_x, float* recv_scale, int32_t* recv_src);
+
+/* Combine over dedup rows, in two stages.  Stage 1 (receiver side): each
+ * dedup row (t, r) gets partial = bf16_rn( sum over the token's valid pairs j
+ * on rank r, in j order, of w[t][j] * y[row[t][j]] ) -- the BF16 weighted sum
+ * of the rank's expert outputs that combine sends back ("NVSHMEM 与 DeepEP",
+ * "高吞吐模式": combine returns BF16 weighted sums).  Stage 2 (source side):
+ * out[t] = bf16_rn( exact sum of the token's partials ).  Sums in binary64.
+ * tokens / ntok as orc_combine; partial [nd][H] may be NULL. */
+int orc_combine_dedup(const uint16_t* y, int64_t nrows, int H, const int32_t* topk_idx,
+                      const int32_t* row, const float* w, int64_t T, int k, int E, int R,
+                      const int32_t* drow, int64_t nd, const int64_t* tokens, int64_t ntok,
+                      uint16_t* partial, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif
