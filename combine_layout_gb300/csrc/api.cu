@@ -41,6 +41,15 @@ struct moe_ep_handle {
     uint8_t* ntile_cnt;    // [ngroups_max][R][16]
     int32_t* ngrp_base;    // [ngroups_max][R]
     unsigned* ndone;
+    // per-rank dedup layout workspace (columns = ranks)
+    uint32_t* rtile_word;  // [ntiles_max][R]
+    uint8_t* rtile_cnt;    // [ngroups_max][R][16]
+    int32_t* rgrp_base;    // [ngroups_max][R]
+    unsigned* rdone;
+    int32_t* rk_cnt;       // [R] tokens per destination rank
+    int32_t* rk_off;       // [R+1]
+    int32_t* drow;         // [max_tokens * max_topk] dedup row of each pair (-1: not its rank's first)
+    int dedup_ready;       // the dedup layout and row map belong to the last route
     // counts published by the layout for the receive-count query (mapped
     // pinned memory): off[E+1], rcnt[R], cnt[E], then the sequence number of
     // the route that wrote them
@@ -79,6 +88,13 @@ T* carve(char*& cur, size_t count)
     size_t bytes = (sizeof(T) * count + 255) & ~(size_t)255;
     cur += bytes;
     return p;
+}
+
+// Dedup rows a route can need: one per (token, destination rank).
+int64_t dedup_capacity(const moe_ep_handle* h)
+{
+    const int k = h->k, R = h->g->R;
+    return (int64_t)h->T * (k < R ? k : R);
 }
 
 int64_t required_rows(const moe_ep_handle* h)
@@ -122,6 +138,9 @@ RowArgs row_args(const moe_ep_handle* h)
     a.E = h->g->E;
     a.S = h->g->S;
     a.mode = h->g->mode;
+    a.G = 1;
+    a.ncols = a.E;
+    a.mask = nullptr;
     return a;
 }
 
@@ -219,10 +238,12 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     const size_t ntn = (size_t)h->ntiles_max * g->R;
     const size_t cstride = ((size_t)h->ntiles_max + 15) / 16 * 16;
     const size_t ngrp = cstride / 16;
-    const size_t counts[15] = {nt, ngrp * g->E, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+    const size_t counts[21] = {nt, ngrp * g->E, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
                                (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1,
                                (size_t)g->E * cstride / 4,
-                               ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1, 0};
+                               ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1,
+                               ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1, (size_t)g->R,
+                               (size_t)g->R + 1, (size_t)g->S * max_topk};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -245,6 +266,13 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->ntile_cnt = carve<uint8_t>(cur, (size_t)g->R * cstride);
     h->ngrp_base = carve<int32_t>(cur, counts[12]);
     h->ndone = carve<unsigned>(cur, 1);
+    h->rtile_word = carve<uint32_t>(cur, counts[14]);
+    h->rtile_cnt = carve<uint8_t>(cur, (size_t)g->R * cstride);
+    h->rgrp_base = carve<int32_t>(cur, counts[16]);
+    h->rdone = carve<unsigned>(cur, 1);
+    h->rk_cnt = carve<int32_t>(cur, counts[18]);
+    h->rk_off = carve<int32_t>(cur, counts[19]);
+    h->drow = carve<int32_t>(cur, counts[20]);
     if (cudaMemset(base, 0, bytes) != cudaSuccess) {
         cudaFree(base);
         delete h;
@@ -277,6 +305,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->has_sent = 0;
     h->routed = 0;
     h->rows_ready = 0;
+    h->dedup_ready = 0;
     h->host_total = -1;
     h->align = 1;
     g->handles += 1;
@@ -356,6 +385,7 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (la.host_out) h->seq = la.seq;
     h->routed = 1;
     h->rows_ready = 0;
+    h->dedup_ready = 0;
     h->T = T;
     h->k = k;
     h->host_total = -1;
@@ -575,6 +605,159 @@ int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node, int32_t* 
     la.align = 1;
     return cuda_status(launch_node_layout(a, la, reinterpret_cast<unsigned long long*>(stats),
                                           node_src, node_mask, g->sm_count, s));
+}
+
+int moe_ep_dispatch_dedup(moe_ep_handle_t h, const void* x, int fp8, void* drecv_x,
+                          float* drecv_scale, int32_t* drecv_src, uint32_t* drecv_mask,
+                          int32_t* rank_cnt, int32_t* rank_off, int64_t drecv_rows,
+                          moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->routed || g->mode != MOE_EP_HT || g->L > 32) return MOE_EP_ERR_INVALID;
+    if (drecv_rows < dedup_capacity(h)) return MOE_EP_ERR_INVALID;
+    if (h->T > 0 && (!x || !drecv_x || !aligned16(x) || !aligned16(drecv_x)))
+        return MOE_EP_ERR_INVALID;
+    if (fp8) {
+        if (g->H % 128 != 0) return MOE_EP_ERR_INVALID;
+        if (h->T > 0 && (!drecv_scale || ((uintptr_t)drecv_scale & 3u))) return MOE_EP_ERR_INVALID;
+    }
+    if (((uintptr_t)drecv_src & 3u) || ((uintptr_t)drecv_mask & 3u) ||
+        ((uintptr_t)rank_cnt & 3u) || ((uintptr_t)rank_off & 3u))
+        return MOE_EP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int T = h->T;
+    cudaError_t e = cudaSuccess;
+    if (T == 0) {
+        e = cudaMemsetAsync(h->rk_cnt, 0, sizeof(int32_t) * g->R, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->rk_off, 0, sizeof(int32_t) * (g->R + 1), s);
+    } else {
+        // the layout over ranks: the node layout with one "GPU" per expert and
+        // one "node" per rank (GPU mask bits = local experts)
+        NodeArgs na;
+        na.idx = h->idx;
+        na.T = T;
+        na.k = h->k;
+        na.E = g->E;
+        na.L = 1;
+        na.gpn = g->L;
+        na.N = g->R;
+        na.src = 0;
+        LayoutArgs la;
+        la.tile_word = h->rtile_word;
+        la.tile_cnt = h->rtile_cnt;
+        la.grp_base = h->rgrp_base;
+        la.cnt = h->rk_cnt;
+        la.off = h->rk_off;
+        la.rcnt = h->rk_cnt;  // one "rank" per column: the same sums
+        la.roff = h->rk_off;
+        la.done = h->rdone;
+        la.E = g->R;
+        la.R = g->R;
+        la.ntiles = (T + kTileTokens - 1) / kTileTokens;
+        la.host_out = nullptr;
+        la.seq = 0u;
+        la.align = 1;
+        e = launch_node_layout(na, la, nullptr, nullptr, nullptr, g->sm_count, s);
+        if (e == cudaSuccess) {
+            RowArgs ra;
+            ra.idx = h->idx;
+            ra.tile_word = h->rtile_word;
+            ra.tile_cnt = h->rtile_cnt;
+            ra.grp_base = h->rgrp_base;
+            ra.off = h->rk_off;
+            ra.T = T;
+            ra.k = h->k;
+            ra.E = g->E;
+            ra.S = g->S;
+            ra.mode = MOE_EP_HT;
+            ra.G = g->L;
+            ra.ncols = g->R;
+            ra.mask = drecv_mask;
+            e = launch_dispatch(ra, x, g->H, fp8, h->drow, drecv_x, drecv_scale, drecv_src,
+                                nullptr, nullptr, g->sm_count, s);
+        }
+    }
+    if (e == cudaSuccess && rank_cnt)
+        e = cudaMemcpyAsync(rank_cnt, h->rk_cnt, sizeof(int32_t) * g->R, cudaMemcpyDefault, s);
+    if (e == cudaSuccess && rank_off)
+        e = cudaMemcpyAsync(rank_off, h->rk_off, sizeof(int32_t) * (g->R + 1), cudaMemcpyDefault, s);
+    if (e != cudaSuccess) return MOE_EP_ERR_CUDA;
+    h->dedup_ready = 1;
+    return MOE_EP_OK;
+}
+
+int moe_ep_expand(moe_ep_handle_t h, const void* drecv_x, const float* drecv_scale,
+                  const int32_t* drecv_src, const uint32_t* drecv_mask, int fp8, void* recv_x,
+                  float* recv_scale, int32_t* recv_src, int64_t recv_rows, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->dedup_ready) return MOE_EP_ERR_INVALID;
+    if (recv_rows < required_rows(h)) return MOE_EP_ERR_INVALID;
+    if (h->T == 0) return MOE_EP_OK;
+    if (!drecv_x || !drecv_src || !drecv_mask || !recv_x || !aligned16(drecv_x) ||
+        !aligned16(recv_x) || ((uintptr_t)drecv_src & 3u) || ((uintptr_t)drecv_mask & 3u) ||
+        ((uintptr_t)recv_src & 3u))
+        return MOE_EP_ERR_INVALID;
+    if (fp8 && (g->H % 128 != 0 || !drecv_scale || !recv_scale ||
+                ((uintptr_t)drecv_scale & 3u) || ((uintptr_t)recv_scale & 3u)))
+        return MOE_EP_ERR_INVALID;
+    DedupArgs a;
+    a.ex = row_args(h);
+    a.rank_off = h->rk_off;
+    a.dsrc = drecv_src;
+    a.dmask = drecv_mask;
+    a.R = g->R;
+    a.L = g->L;
+    const int row_bytes = fp8 ? g->H : 2 * g->H;
+    return cuda_status(launch_expand(a, drecv_x, fp8 ? drecv_scale : nullptr, row_bytes,
+                                     g->H / 128, recv_x, fp8 ? recv_scale : nullptr, recv_src,
+                                     (int)dedup_capacity(h), g->sm_count, (cudaStream_t)stream));
+}
+
+int moe_ep_combine_dedup(moe_ep_handle_t h, const void* y, const float* topk_w,
+                         const int32_t* drecv_src, void* partial, void* out, int64_t recv_rows,
+                         int64_t drecv_rows, moe_ep_stream_t stream)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    moe_ep_group* g = h->g;
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!h->dedup_ready) return MOE_EP_ERR_INVALID;
+    if (recv_rows < required_rows(h) || drecv_rows < dedup_capacity(h)) return MOE_EP_ERR_INVALID;
+    if (h->T == 0) return MOE_EP_OK;
+    if (!y || !topk_w || !drecv_src || !partial || !out || !aligned16(y) || !aligned16(partial) ||
+        !aligned16(out) || ((uintptr_t)topk_w & 3u) || ((uintptr_t)drecv_src & 3u))
+        return MOE_EP_ERR_INVALID;
+    // the partial rows must not overlap y or out
+    const size_t rb = (size_t)g->H * 2;
+    const char* pb = (const char*)partial;
+    const char* pe = pb + (size_t)drecv_rows * rb;
+    const char* yb = (const char*)y;
+    const char* ye = yb + (size_t)recv_rows * rb;
+    const char* ob = (const char*)out;
+    const char* oe = ob + (size_t)h->T * rb;
+    if ((pb < ye && yb < pe) || (pb < oe && ob < pe) || (ob < ye && yb < oe))
+        return MOE_EP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    DedupArgs a;
+    a.ex = row_args(h);
+    a.rank_off = h->rk_off;
+    a.dsrc = drecv_src;
+    a.dmask = nullptr;
+    a.R = g->R;
+    a.L = g->L;
+    st = cuda_status(launch_combine_partial(a, topk_w, y, g->H, partial, (int)dedup_capacity(h),
+                                            g->sm_count, s));
+    if (st != MOE_EP_OK) return st;
+    // the source adds its ranks' partial rows: weights 1, dedup row map
+    return cuda_status(launch_combine(partial, h->T, g->H, h->k, h->drow, nullptr, out,
+                                      g->sm_count, s));
 }
 
 int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* rcnt, int32_t* roff,

@@ -7,39 +7,19 @@
 // back is the weighted sum of the expert outputs, kept in BF16.
 //
 // out[t][h] = bf16_rn(fma(w_{k-1}, y_{k-1}, ... fma(w_1, y_1, fma(w_0, y_0, 0)))),
-// fp32 accumulation in fixed j order, so results do not depend on scheduling.
+// fp32 accumulation in fixed j order, so results do not depend on scheduling
+// (w == nullptr: every weight 1, a plain sum -- the source-side stage of the
+// per-rank dedup combine, which adds each rank's partial row).
 // HBM-bound: k gathered row reads and one row write per token; a CTA takes
 // one token at a time, every thread issuing the loads of all k rows for its
 // 16-byte slice before accumulating.
-#include <cuda_bf16.h>
-
+#include "bf16x8.cuh"
 #include "common.cuh"
 
 namespace moeep {
 namespace {
 
 constexpr int kThreads = 128;
-
-__device__ __forceinline__ void acc8(float (&a)[8], float w, const uint4& v)
-{
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        a[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), a[2 * i]);
-        a[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xffff0000u), a[2 * i + 1]);
-    }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&a)[8])
-{
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
-        o[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
 
 // Register budget per row count: enough CTAs per SM to keep the gathered rows
 // of many tokens in flight (k <= 8: 64 registers, 8 CTAs -- measured on the
@@ -60,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         if (threadIdx.x < k) {
             s_row[threadIdx.x] = row[(size_t)t * k + threadIdx.x];
-            s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+            s_w[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
         }
         __syncthreads();
         int r[KMAX];

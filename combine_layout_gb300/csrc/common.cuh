@@ -94,7 +94,9 @@ struct LayoutArgs {
     unsigned seq;
 };
 
-// What placing a pair into its receive row needs.
+// What placing a pair into its receive row needs.  Columns of the layout are
+// blocks of G consecutive experts (G = 1: experts; G = E/R: ranks, one row
+// per (token, rank) at the token's first pair on that rank).
 struct RowArgs {
     const int32_t* idx;        // handle copy of topk_idx [T][k]
     const uint32_t* tile_word;
@@ -102,6 +104,19 @@ struct RowArgs {
     const int32_t* grp_base;
     const int32_t* off;
     int T, k, E, S, mode;
+    int G;                     // experts per column
+    int ncols;                 // E / G
+    uint32_t* mask;            // G > 1: per row, bit l = local expert l of the token (may be null)
+};
+
+// What the receiver side of the per-rank dedup path needs: the expert layout
+// (G = 1) and the dedup rows' ranks, tokens and local-expert masks.
+struct DedupArgs {
+    RowArgs ex;
+    const int32_t* rank_off;  // [R+1]
+    const int32_t* dsrc;      // [dedup rows] token
+    const uint32_t* dmask;    // [dedup rows] bit l: local expert l of the row's rank
+    int R, L;
 };
 
 // What the node-level layout needs.
@@ -136,6 +151,7 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
 
 // Node-level layout (node counts, offsets, rows with GPU masks) and the
 // routing statistics (stats may be null; otherwise 4 sums, accumulated).
+// node_src == nullptr: the layout (counts, offsets, tile words) only.
 cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned long long* stats,
                                int32_t* node_src, uint32_t* node_mask, int sm_count, cudaStream_t s);
 
@@ -145,7 +161,17 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
                            const uint8_t* q, const float* scale, void* y, int sm_count,
                            cudaStream_t s);
 
-// Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]).
+// Per-rank dedup, receiver side: copy every dedup row to the HT rows of its
+// local experts (row_bytes per row, nblk scales per row when dscale is set),
+// and the per-rank BF16 partial weighted sums.  max_rows bounds the grid;
+// the kernels read the number of dedup rows from rank_off[R].
+cudaError_t launch_expand(const DedupArgs& a, const void* dx, const float* dscale, int row_bytes,
+                          int nblk, void* recv_x, float* recv_scale, int32_t* recv_src,
+                          int max_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_combine_partial(const DedupArgs& a, const float* w, const void* y, int H,
+                                   void* partial, int max_rows, int sm_count, cudaStream_t s);
+
+// Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]) (w == nullptr: weights 1).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,
                            void* out, int sm_count, cudaStream_t s);
 

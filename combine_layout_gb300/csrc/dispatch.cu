@@ -34,11 +34,13 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
 {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        const int r = token_pair_row(ra, t, lane);
+        uint32_t m = 0u;
+        const int r = token_pair_row(ra, t, lane, &m);
         if (lane < ra.k) {
             s_row[lane] = r;
             row[(size_t)t * ra.k + lane] = r;
             if (r >= 0 && recv_src) recv_src[r] = t;
+            if (r >= 0 && ra.mask) ra.mask[r] = m;
         }
     }
 }

@@ -12,7 +12,8 @@ __global__ void __launch_bounds__(256) rowmap_kernel(RowArgs a, int32_t* __restr
     const int lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
     for (int t = blockIdx.x * wpc + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpc) {
-        const int r = token_pair_row(a, t, lane);
+        uint32_t m = 0u;
+        const int r = token_pair_row(a, t, lane, &m);
         if (lane < a.k) row[(size_t)t * a.k + lane] = r;
     }
 }

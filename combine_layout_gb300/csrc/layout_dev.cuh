@@ -257,18 +257,36 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
 // Receive row of pair (t, lane) for lanes < k of a warp (-1 for lanes >= k and
 // for pairs without a row).  All 32 lanes must call it (warp-collective).
 // Invalid pairs -- id outside [0, E), or an expert repeated at an earlier j of
-// the same token -- get -1.
-__device__ __forceinline__ int token_pair_row(const RowArgs& a, int t, int lane)
+// the same token -- get -1.  With G > 1 experts per column only the token's
+// first valid pair in each column gets the row, and *mask receives the bits
+// e % G of all the token's valid experts in that column.
+__device__ __forceinline__ int token_pair_row(const RowArgs& a, int t, int lane, uint32_t* mask)
 {
+    const unsigned full = 0xffffffffu, lower = (1u << lane) - 1u;
     int e = -2 - lane;  // lanes >= k: distinct values that match nothing
     if (lane < a.k) e = __ldg(a.idx + (size_t)t * a.k + lane);
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const bool dup = (peers & ((1u << lane) - 1u)) != 0u;
-    if (lane >= a.k || e < 0 || e >= a.E || dup) return -1;
+    const unsigned peers = __match_any_sync(full, e);
+    const bool valid = lane < a.k && e >= 0 && e < a.E && (peers & lower) == 0u;
+    int col = e;
+    uint32_t m = 1u;
+    if (a.G > 1) {  // warp-uniform
+        col = valid ? e / a.G : -100 - lane;
+        const unsigned cpeers = __match_any_sync(full, col);
+        const uint32_t bit = valid ? 1u << (e - col * a.G) : 0u;
+        m = 0u;
+        for (int j = 0; j < a.k; ++j) {
+            const uint32_t b = __shfl_sync(full, bit, j);
+            if ((cpeers >> j) & 1u) m |= b;
+        }
+        if ((cpeers & lower) != 0u) return -1;  // a lower lane holds this column
+    }
+    *mask = m;
+    if (!valid) return -1;
     const int tile = t / kTileTokens;
-    const int rank = pairs_before_tile(a.tile_cnt, a.grp_base, a.E, e, tile) +
-                     __popc(__ldg(a.tile_word + (size_t)tile * a.E + e) & ((1u << (t & 31)) - 1u));
-    return (a.mode == MOE_EP_HT) ? __ldg(a.off + e) + rank : e * a.S + rank;
+    const int rank =
+        pairs_before_tile(a.tile_cnt, a.grp_base, a.ncols, col, tile) +
+        __popc(__ldg(a.tile_word + (size_t)tile * a.ncols + col) & ((1u << (t & 31)) - 1u));
+    return (a.mode == MOE_EP_HT) ? __ldg(a.off + col) + rank : col * a.S + rank;
 }
 
 }  // namespace moeep

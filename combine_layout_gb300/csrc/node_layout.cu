@@ -121,7 +121,7 @@ cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned
     if (a.T <= 0) return cudaSuccess;
     cudaError_t e = launch_pdl(node_bits_kernel, dim3(la.ntiles), dim3(kThreads), s, a,
                                tail_planned(la, kThreads), stats);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || !node_src) return e;  // no node_src: the layout only
     int blocks = (a.T + 7) / 8;
     if (blocks > sm_count * 8) blocks = sm_count * 8;
     return launch_pdl(node_rows_kernel, dim3(blocks), dim3(kThreads), s, a,

@@ -148,6 +148,9 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     ra.E = experts;
     ra.S = slots;
     ra.mode = mode;
+    ra.G = 1;
+    ra.ncols = experts;
+    ra.mask = nullptr;
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

@@ -62,6 +62,9 @@ def _load() -> ctypes.CDLL:
         "moe_ep_dequant": [P, P, P, P, I64, P],
         "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
                                        P, P, P],
+        "moe_ep_dispatch_dedup": [P, P, I, P, P, P, P, P, P, I64, P],
+        "moe_ep_expand": [P, P, P, P, P, I, P, P, P, I64, P],
+        "moe_ep_combine_dedup": [P, P, P, P, P, P, I64, I64, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -223,6 +226,42 @@ def moe_ep_node_layout(handle: int, num_nodes: int, src_node: int, node_cnt, nod
            _lib.moe_ep_node_layout(ctypes.c_void_p(handle), num_nodes, src_node, _ptr(node_cnt),
                                    _ptr(node_off), _ptr(node_src), _ptr(node_mask), node_rows,
                                    _ptr(stats), _stream(stream)))
+
+
+def moe_ep_dispatch_dedup(handle: int, x, fp8: bool, drecv_x, drecv_scale=None, drecv_src=None,
+                          drecv_mask=None, rank_cnt=None, rank_off=None,
+                          drecv_rows: int | None = None, stream=None) -> None:
+    if drecv_rows is None:
+        drecv_rows = drecv_x.shape[0]
+    _check("moe_ep_dispatch_dedup",
+           _lib.moe_ep_dispatch_dedup(ctypes.c_void_p(handle), _ptr(x), int(bool(fp8)),
+                                      _ptr(drecv_x), _ptr(drecv_scale), _ptr(drecv_src),
+                                      _ptr(drecv_mask), _ptr(rank_cnt), _ptr(rank_off),
+                                      drecv_rows, _stream(stream)))
+
+
+def moe_ep_expand(handle: int, drecv_x, drecv_scale, drecv_src, drecv_mask, fp8: bool, recv_x,
+                  recv_scale=None, recv_src=None, recv_rows: int | None = None,
+                  stream=None) -> None:
+    if recv_rows is None:
+        recv_rows = recv_x.shape[0]
+    _check("moe_ep_expand",
+           _lib.moe_ep_expand(ctypes.c_void_p(handle), _ptr(drecv_x), _ptr(drecv_scale),
+                              _ptr(drecv_src), _ptr(drecv_mask), int(bool(fp8)), _ptr(recv_x),
+                              _ptr(recv_scale), _ptr(recv_src), recv_rows, _stream(stream)))
+
+
+def moe_ep_combine_dedup(handle: int, y, topk_w, drecv_src, partial, out,
+                         recv_rows: int | None = None, drecv_rows: int | None = None,
+                         stream=None) -> None:
+    if recv_rows is None:
+        recv_rows = y.shape[0]
+    if drecv_rows is None:
+        drecv_rows = partial.shape[0]
+    _check("moe_ep_combine_dedup",
+           _lib.moe_ep_combine_dedup(ctypes.c_void_p(handle), _ptr(y), _ptr(topk_w),
+                                     _ptr(drecv_src), _ptr(partial), _ptr(out), recv_rows,
+                                     drecv_rows, _stream(stream)))
 
 
 def moe_ep_get_device_errors(group: int) -> int:

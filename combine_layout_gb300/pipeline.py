@@ -73,6 +73,43 @@ class EpPipeline:
         ep.moe_ep_dequant(self.handle, self.recv_x, self.recv_scale, y, self.rows, stream)
         return y
 
+    # ------------------------------------------------- per-rank dedup (HT)
+    def _dedup_buffers(self):
+        if getattr(self, "drows", None) is None:
+            dev = self.device
+            self.drows = self.S * min(self.k, self.R)
+            self.drecv_x = torch.empty((self.drows, self.H),
+                                       dtype=torch.uint8 if self.fp8 else torch.bfloat16, device=dev)
+            self.drecv_scale = (torch.empty((self.drows, self.H // 128), dtype=torch.float32,
+                                            device=dev) if self.fp8 else None)
+            self.drecv_src = torch.empty(self.drows, dtype=torch.int32, device=dev)
+            self.drecv_mask = torch.empty(self.drows, dtype=torch.int32, device=dev)
+            self.rank_cnt = torch.empty(self.R, dtype=torch.int32, device=dev)
+            self.rank_off = torch.empty(self.R + 1, dtype=torch.int32, device=dev)
+            self.partial = torch.empty((self.drows, self.H), dtype=torch.bfloat16, device=dev)
+
+    def dispatch_dedup(self, x, stream=None):
+        """One copy per (token, destination rank) into drecv_*; rank_cnt / rank_off."""
+        self._dedup_buffers()
+        ep.moe_ep_dispatch_dedup(self.handle, x, self.fp8, self.drecv_x, self.drecv_scale,
+                                 self.drecv_src, self.drecv_mask, self.rank_cnt, self.rank_off,
+                                 self.drows, stream)
+
+    def expand(self, stream=None):
+        """Receiver side: the dedup rows into recv_x / recv_scale / recv_src."""
+        ep.moe_ep_expand(self.handle, self.drecv_x, self.drecv_scale, self.drecv_src,
+                         self.drecv_mask, self.fp8, self.recv_x, self.recv_scale, self.recv_src,
+                         self.rows, stream)
+
+    def combine_dedup(self, y, topk_w=None, out=None, stream=None):
+        if topk_w is None:
+            topk_w = self.topk_w
+        if out is None:
+            out = self.out
+        ep.moe_ep_combine_dedup(self.handle, y, topk_w, self.drecv_src, self.partial, out,
+                                y.shape[0], self.drows, stream)
+        return out[: self.T]
+
     def layout(self, stream=None) -> dict:
         dev = self.device
         L = dict(cnt=torch.empty(self.E, dtype=torch.int32, device=dev),

@@ -250,6 +250,73 @@ MOE_EP_API int moe_ep_node_layout(moe_ep_handle_t h, int num_nodes, int src_node
                                   uint32_t* node_mask, int64_t node_rows, int64_t* stats,
                                   moe_ep_stream_t stream);
 
+/* Per-rank dedup dispatch (HT mode): one copy of a token per destination rank
+ * holding at least one of its experts, instead of one per expert -- the
+ * page's copies by destination GPU ("NVSHMEM 与 DeepEP：GPU 发起的通信", section
+ * "高吞吐模式", routing simulation: "按目标卡去重"), the receive format of DeepEP's
+ * normal mode.  Rows are rank-major with tokens ascending; each carries its
+ * token and the mask of the rank's local experts it must reach.
+ * x           device bf16 [T][H] (16-byte aligned), as moe_ep_dispatch.
+ * fp8         0: drecv_x bf16 [drecv_rows][H]; 1: drecv_x e4m3 [drecv_rows][H]
+ *             with drecv_scale fp32 [drecv_rows][H/128] (the same per-128
+ *             quantisation as moe_ep_dispatch).
+ * drecv_src   device int32 [drecv_rows]: token of each dedup row (or NULL).
+ * drecv_mask  device uint32 [drecv_rows]: bit l set when local expert l of the
+ *             row's rank (expert r * E/R + l) is one of the token's experts
+ *             (or NULL).
+ * rank_cnt    device int32 [R] (or NULL): dedup rows per rank.
+ * rank_off    device int32 [R+1] (or NULL): exclusive prefix; rank_off[R] is
+ *             the number of dedup rows.
+ * drecv_rows  capacity: at least T * min(k, R).
+ * The handle keeps the rank layout and the dedup row of every (token, pair)
+ * for moe_ep_expand and moe_ep_combine_dedup; the next moe_ep_route clears it.
+ * Masked (-1), invalid and repeated expert ids are skipped as in the layout.
+ * Errors: MOE_EP_ERR_INVALID in LL mode, for E/R > 32, too small drecv_rows,
+ * misaligned pointers, or no preceding moe_ep_route. */
+MOE_EP_API int moe_ep_dispatch_dedup(moe_ep_handle_t h, const void* x, int fp8, void* drecv_x,
+                                     float* drecv_scale, int32_t* drecv_src,
+                                     uint32_t* drecv_mask, int32_t* rank_cnt, int32_t* rank_off,
+                                     int64_t drecv_rows, moe_ep_stream_t stream);
+
+/* Receiver side of the dedup dispatch: every dedup row is copied, bytes as
+ * they are (bf16, or e4m3 with its scales), to the expert-major HT receive
+ * row of each local expert in its mask -- the rows moe_ep_dispatch writes, so
+ * recv_x / recv_scale / recv_src equal the direct dispatch's output bit for
+ * bit.  Inputs are the outputs of the last moe_ep_dispatch_dedup on this
+ * handle (drecv_x, drecv_scale when fp8, drecv_src, drecv_mask); recv_x etc.
+ * as moe_ep_dispatch (recv_src may be NULL), recv_rows at least what
+ * moe_ep_dispatch requires.  No host synchronisation: the number of dedup
+ * rows is read on the device.  Errors: MOE_EP_ERR_INVALID without a
+ * preceding moe_ep_dispatch_dedup for the current route, for misaligned or
+ * missing buffers, or too few rows. */
+MOE_EP_API int moe_ep_expand(moe_ep_handle_t h, const void* drecv_x, const float* drecv_scale,
+                             const int32_t* drecv_src, const uint32_t* drecv_mask, int fp8,
+                             void* recv_x, float* recv_scale, int32_t* recv_src,
+                             int64_t recv_rows, moe_ep_stream_t stream);
+
+/* Combine over the dedup rows, in two stages ("NVSHMEM 与 DeepEP", "高吞吐模式":
+ * combine sends back BF16 weighted sums of the expert outputs).  Receiver
+ * side: each dedup row (token t, rank r) gets
+ *   partial = bf16_rn( fma chain in j order over t's valid pairs j on rank r
+ *                      of topk_w[t][j] * y[row(t, j)] )   (fp32);
+ * source side: out[t] = bf16_rn( sum of t's partial rows, fp32, in the order of
+ * the pairs that carry them ).
+ * y       device bf16 [recv_rows][H] in the expert-major HT layout (16-byte
+ *         aligned), as moe_ep_combine.
+ * topk_w  device fp32 [T][k].
+ * drecv_src the dedup rows' tokens from moe_ep_dispatch_dedup.
+ * partial device bf16 [drecv_rows][H] (16-byte aligned), written: the rows the
+ *         ranks send back.
+ * out     device bf16 [T][H] (16-byte aligned).  partial, y and out must not
+ *         overlap.
+ * Errors: MOE_EP_ERR_INVALID without a preceding moe_ep_dispatch_dedup for the
+ * current route, for misaligned, missing or overlapping buffers, or too few
+ * rows. */
+MOE_EP_API int moe_ep_combine_dedup(moe_ep_handle_t h, const void* y, const float* topk_w,
+                                    const int32_t* drecv_src, void* partial, void* out,
+                                    int64_t recv_rows, int64_t drecv_rows,
+                                    moe_ep_stream_t stream);
+
 /* Copy the handle's layout to caller buffers (device or host pointers; NULL
  * skips an item): cnt [E], off [E+1], rcnt [R], roff [R+1], row [T][k] with -1
  * for pairs without a row.  Asynchronous for device destinations; host

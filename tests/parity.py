@@ -58,3 +58,18 @@ def dequant_on_device(q: torch.Tensor, scale: torch.Tensor, chunk: int = 8192) -
         f = torch.nan_to_num(f * scale[a:b, :, None], nan=0.0, posinf=0.0, neginf=0.0)
         y[a:b] = f.view(b - a, H).to(torch.bfloat16)
     return y
+
+
+def identity_rows(x_bits: np.ndarray, tokens, fp8: bool) -> np.ndarray:
+    """The oracle's expert input for each listed token under identity experts:
+    the token's bf16 row, or (FP8) bf16_rn(float(q) * scale) of the oracle's
+    own quantisation of it.  [len(tokens)][H] bf16 bits, oracle values only."""
+    import oracle
+    rows = []
+    for t in np.asarray(tokens).reshape(-1):
+        if fp8:
+            q, s = oracle.quant_row(x_bits[t])
+            rows.append(oracle.dequant_rows(q[None], s[None], [0])[0])
+        else:
+            rows.append(x_bits[t])
+    return np.stack(rows) if rows else np.zeros((0, x_bits.shape[1]), np.uint16)

@@ -82,10 +82,11 @@ def test_masked_pairs_get_no_row_and_no_term():
     assert st == oracle.OK and total == int((idx >= 0).sum())
     assert np.array_equal(p.layout()["row"].cpu().numpy(), L_o["row"])
     p.dispatch(to_dev_bf16(x, DEV))
-    w = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(DEV)
-    out = p.combine(p.recv_x, w)
+    w_h = rng.random((T, k)).astype(np.float32)
+    out = p.combine(p.recv_x, torch.from_numpy(w_h).to(DEV))
     torch.cuda.synchronize()
-    want = oracle.combine(bf16_bits(p.recv_x), L_o["row"], w.cpu().numpy())
+    y_o, _, _ = oracle.dispatch(x, L_o["row"], total, fp8=False)
+    want = oracle.combine(y_o, L_o["row"], w_h)
     assert bf16_ulp_diff(bf16_bits(out), want).max() <= 1
     assert np.all(bf16_bits(out)[7] == 0)
     assert p.device_errors() == 0

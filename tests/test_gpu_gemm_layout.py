@@ -42,8 +42,9 @@ def test_aligned_layout_and_round_trip(name, T, align):
     p.dispatch(to_dev_bf16(inp["x"], DEV))
     out = p.combine(p.recv_x)
     torch.cuda.synchronize()
-    idx = p.topk_idx[:T].cpu().numpy()
-    L_o, st = oracle.layout(idx, w.E, w.R, oracle.MODE_HT, align=align)
+    idx_o, _ = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+    assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
+    L_o, st = oracle.layout(idx_o, w.E, w.R, oracle.MODE_HT, align=align)
     assert st == oracle.OK
     L = {k_: v.cpu().numpy() for k_, v in p.layout().items()}
     for key in ("cnt", "off", "rcnt", "roff", "row"):
@@ -71,11 +72,12 @@ def test_dequant_matches_oracle(name, T, align):
     y.view(torch.int16).fill_(SENT)
     p.dequant(y)
     torch.cuda.synchronize()
-    idx = p.topk_idx[:T].cpu().numpy()
-    L_o, _ = oracle.layout(idx, w.E, w.R, w.mode, w.slots, align=align)
+    idx_o, _ = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+    assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
+    L_o, _ = oracle.layout(idx_o, w.E, w.R, w.mode, w.slots, align=align)
     rows = _defined_rows(w, L_o)
-    q = p.recv_x.cpu().numpy()
-    sc = p.recv_scale.cpu().numpy()
+    # the oracle dequantises its own FP8 dispatch of the same tokens
+    q, sc, _ = oracle.dispatch(inp["x"], L_o["row"], p.rows, fp8=True)
     want = oracle.dequant_rows(q, sc, rows)
     got = bf16_bits(y)
     assert np.array_equal(got[rows], want[rows])

@@ -47,8 +47,9 @@ def test_page_simulation_statistics_on_device():
         p = EpPipeline(synth.MODE_HT, 256, 64, 4096, 128, 8, device=DEV)
         p.route(torch.from_numpy(s).to(DEV), 4096, G, kg, 2)
         got = _node_layout(p, 8, 0)
-        idx = p.topk_idx[:4096].cpu().numpy()
-        _check(got, oracle.node_layout(idx, 256, 64, 8, 0))
+        idx_o, _ = oracle.route(s, 8, G, kg, group_topk=2)
+        assert np.array_equal(p.topk_idx[:4096].cpu().numpy(), idx_o)
+        _check(got, oracle.node_layout(idx_o, 256, 64, 8, 0))
         per_tok = (got["stats"] / 4096.0).tolist()
         assert [f"{v:.2f}" for v in per_tok] == [f"{v:.2f}" for v in golden[name][:4]], name
         p.close()
@@ -64,8 +65,9 @@ def test_node_layout_matches_oracle(name, T, N, src):
     p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, 128, w.k, device=DEV)
     p.route(torch.from_numpy(inp["scores"]).to(DEV), T, w.G, w.kg, 0, w.weight_mode)
     got = _node_layout(p, N, src)
-    idx = p.topk_idx[:T].cpu().numpy()
-    _check(got, oracle.node_layout(idx, w.E, w.R, N, src))
+    idx_o, _ = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+    assert np.array_equal(p.topk_idx[:T].cpu().numpy(), idx_o)
+    _check(got, oracle.node_layout(idx_o, w.E, w.R, N, src))
     p.close()
 
 

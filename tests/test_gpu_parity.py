@@ -15,7 +15,8 @@ import torch
 
 import oracle
 from combine_layout_gb300 import synth
-from parity import W_RTOL, bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device, to_dev_bf16
+from parity import (W_RTOL, bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device,
+                    identity_rows, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +39,7 @@ def _check_route_layout(w, p, inp):
     assert st == oracle.OK
     for key in ("cnt", "off", "rcnt", "roff", "row"):
         assert np.array_equal(L[key], L_o[key]), key
-    return idx_o, wg, L_o
+    return idx_o, w_o, L_o
 
 
 def _run(w, sample=None, seed=None):
@@ -50,7 +51,7 @@ def _run(w, sample=None, seed=None):
     total, per_rank, per_expert = p.num_recv_tokens()
     p.dispatch(x)
     torch.cuda.synchronize()
-    idx_o, wg, L_o = _check_route_layout(w, p, inp)
+    idx_o, w_o, L_o = _check_route_layout(w, p, inp)
 
     if w.mode == synth.MODE_HT:
         assert total == w.T * w.k
@@ -85,20 +86,21 @@ def _run(w, sample=None, seed=None):
         assert np.array_equal(got, inp["x"][want_src[rows]]), "bf16 payload differs"
         y = p.recv_x
 
-    out = p.combine(y)
+    # both sides combine with the oracle's gate weights (fp32)
+    w32 = np.zeros((w.T, w.k), np.float32)
+    w32[:] = w_o
+    out = p.combine(y, topk_w=torch.from_numpy(w32).to(DEV))
     torch.cuda.synchronize()
     tokens = np.arange(w.T)
     if sample is not None and w.T > sample:
         rng = np.random.default_rng(7)
         tokens = np.unique(np.concatenate([tokens[:32], tokens[-32:], rng.choice(w.T, sample)]))
-    # the oracle sees exactly the rows these tokens read, compacted
+    # the oracle's own expert input for every pair of these tokens (identity
+    # experts: the token, or its FP8 round trip), rows compacted
     r = L_o["row"][tokens]
-    flat = r.ravel()
-    valid = flat >= 0
-    gather = torch.from_numpy(np.where(valid, flat, 0).astype(np.int64)).to(DEV)
-    y_c = bf16_bits(y.index_select(0, gather))
-    row_c = np.where(valid, np.arange(flat.size), -1).reshape(r.shape).astype(np.int32)
-    want = oracle.combine(y_c, row_c, wg[tokens])
+    y_c = np.repeat(identity_rows(inp["x"], tokens, w.fp8), w.k, axis=0)
+    row_c = np.where(r.ravel() >= 0, np.arange(r.size), -1).reshape(r.shape).astype(np.int32)
+    want = oracle.combine(y_c, row_c, w32[tokens])
     got = bf16_bits(out[torch.from_numpy(tokens).to(DEV)])
     d = bf16_ulp_diff(got, want)
     assert d.max() <= 1, f"combine differs by {d.max()} bf16 ulp"
