@@ -141,6 +141,7 @@ RowArgs row_args(const moe_ep_handle* h)
     a.G = 1;
     a.ncols = a.E;
     a.mask = nullptr;
+    a.off_out = nullptr;
     return a;
 }
 
@@ -676,14 +677,16 @@ int moe_ep_dispatch_dedup(moe_ep_handle_t h, const void* x, int fp8, void* drecv
             ra.G = g->L;
             ra.ncols = g->R;
             ra.mask = drecv_mask;
+            ra.off_out = rank_off;
             e = launch_dispatch(ra, x, g->H, fp8, h->drow, drecv_x, drecv_scale, drecv_src,
-                                nullptr, nullptr, g->sm_count, s);
+                                h->rk_cnt, rank_cnt, g->sm_count, s);
         }
     }
-    if (e == cudaSuccess && rank_cnt)
-        e = cudaMemcpyAsync(rank_cnt, h->rk_cnt, sizeof(int32_t) * g->R, cudaMemcpyDefault, s);
-    if (e == cudaSuccess && rank_off)
-        e = cudaMemcpyAsync(rank_off, h->rk_off, sizeof(int32_t) * (g->R + 1), cudaMemcpyDefault, s);
+    if (T == 0) {
+        if (e == cudaSuccess && rank_cnt) e = cudaMemsetAsync(rank_cnt, 0, sizeof(int32_t) * g->R, s);
+        if (e == cudaSuccess && rank_off)
+            e = cudaMemsetAsync(rank_off, 0, sizeof(int32_t) * (g->R + 1), s);
+    }
     if (e != cudaSuccess) return MOE_EP_ERR_CUDA;
     h->dedup_ready = 1;
     return MOE_EP_OK;
@@ -745,15 +748,10 @@ int moe_ep_combine_dedup(moe_ep_handle_t h, const void* y, const float* topk_w,
     if ((pb < ye && yb < pe) || (pb < oe && ob < pe) || (ob < ye && yb < oe))
         return MOE_EP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
-    DedupArgs a;
-    a.ex = row_args(h);
-    a.rank_off = h->rk_off;
-    a.dsrc = drecv_src;
-    a.dmask = nullptr;
-    a.R = g->R;
-    a.L = g->L;
-    st = cuda_status(launch_combine_partial(a, topk_w, y, g->H, partial, (int)dedup_capacity(h),
-                                            g->sm_count, s));
+    st = ensure_rows(h, s);
+    if (st != MOE_EP_OK) return st;
+    st = cuda_status(launch_combine_partial(row_args(h), h->row, h->drow, g->L, topk_w, y, g->H,
+                                            partial, g->sm_count, s));
     if (st != MOE_EP_OK) return st;
     // the source adds its ranks' partial rows: weights 1, dedup row map
     return cuda_status(launch_combine(partial, h->T, g->H, h->k, h->drow, nullptr, out,

@@ -107,6 +107,7 @@ struct RowArgs {
     int G;                     // experts per column
     int ncols;                 // E / G
     uint32_t* mask;            // G > 1: per row, bit l = local expert l of the token (may be null)
+    int32_t* off_out;          // dispatch: copy of off[0 .. ncols] (may be null)
 };
 
 // What the receiver side of the per-rank dedup path needs: the expert layout
@@ -168,8 +169,12 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
 cudaError_t launch_expand(const DedupArgs& a, const void* dx, const float* dscale, int row_bytes,
                           int nblk, void* recv_x, float* recv_scale, int32_t* recv_src,
                           int max_rows, int sm_count, cudaStream_t s);
-cudaError_t launch_combine_partial(const DedupArgs& a, const float* w, const void* y, int H,
-                                   void* partial, int max_rows, int sm_count, cudaStream_t s);
+// The partials: for each token (ex.idx, ex.T, ex.k, ex.E), its pairs' expert
+// rows row[t][j], dedup rows drow[t][j] (the first pair of each rank), L
+// experts per rank.
+cudaError_t launch_combine_partial(const RowArgs& ex, const int32_t* row, const int32_t* drow,
+                                   int L, const float* w, const void* y, int H, void* partial,
+                                   int sm_count, cudaStream_t s);
 
 // Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]) (w == nullptr: weights 1).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,

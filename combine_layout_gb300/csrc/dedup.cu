@@ -13,7 +13,7 @@
 //     rank's expert outputs for that token (fp32 fma chain in j order, one
 //     rounding).  The source-side sum of the partials is combine_kernel with
 //     unit weights over the dedup row map.
-// HBM-bound copies and gathers; one CTA per dedup row, 16-byte vectors.
+// HBM-bound copies and gathers with 16-byte vectors.
 #include "bf16x8.cuh"
 #include "layout_dev.cuh"
 
@@ -97,55 +97,64 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(DedupArgs a, const uin
     }
 }
 
-template <int KMAX>  // at most KMAX of a token's experts on one rank
-__global__ void __launch_bounds__(kThreads) combine_partial_kernel(DedupArgs a,
-                                                                   const float* __restrict__ w,
-                                                                   const uint4* __restrict__ y,
-                                                                   int nvec,
-                                                                   uint4* __restrict__ partial)
+// One CTA per token: the token's k expert-output rows are read once and each
+// rank's pairs (in j order) are reduced into that rank's dedup row -- the
+// same partials the ranks would form from their own rows, without a chain of
+// lookups from dedup row back to token before the gathers can start.
+// Register budget: as the combine kernel, enough CTAs per SM to keep many
+// tokens' gathered rows in flight.
+constexpr int partial_min_ctas(int kmax)
+{
+    return kmax <= 2 ? 12 : (kmax <= 4 ? 10 : (kmax <= 8 ? 8 : (kmax <= 16 ? 4 : 2)));
+}
+
+template <int KMAX>  // k <= KMAX
+__global__ void __launch_bounds__(kThreads, partial_min_ctas(KMAX)) combine_partial_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ row,
+    const int32_t* __restrict__ drow, const float* __restrict__ w, int T, int k, int E, int L,
+    const uint4* __restrict__ y, int nvec, uint4* __restrict__ partial)
 {
     griddep_wait();
-    __shared__ int s_row[KMAX];
+    __shared__ int s_row[KMAX];   // expert row of pair j (-1: none)
     __shared__ float s_w[KMAX];
-    const int total = __ldg(a.rank_off + a.R);
-    const int k = a.ex.k;
-    for (int q = blockIdx.x; q < total; q += gridDim.x) {
+    __shared__ int s_lead[KMAX];  // first pair of j's rank (-1: pair without a row)
+    __shared__ int s_q[KMAX];     // dedup row when pair j leads its rank, else -1
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
         if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
             const unsigned lower = (1u << lane) - 1u;
-            const int r = row_rank(a.rank_off, a.R, q, lane);
-            const int t = __ldg(a.dsrc + q);
             int e = -2 - lane;
-            if (lane < k) e = __ldg(a.ex.idx + (size_t)t * k + lane);
+            if (lane < k) e = __ldg(idx + (size_t)t * k + lane);
             const unsigned peers = __match_any_sync(kFull, e);
-            const bool on = lane < k && e >= 0 && e < a.ex.E && (peers & lower) == 0u &&
-                            e / a.L == r;
-            const unsigned b = __ballot_sync(kFull, on);
-            if (on) {
-                const int pos = __popc(b & lower);
-                s_row[pos] = expert_row(a.ex, t, e);
-                s_w[pos] = __ldg(w + (size_t)t * k + lane);
+            const bool valid = lane < k && e >= 0 && e < E && (peers & lower) == 0u;
+            const unsigned rpeers = __match_any_sync(kFull, valid ? e / L : -100 - lane);
+            if (lane < KMAX) {
+                const bool in = lane < k;
+                s_row[lane] = valid ? __ldg(row + (size_t)t * k + lane) : -1;
+                s_w[lane] = in ? __ldg(w + (size_t)t * k + lane) : 0.f;
+                s_lead[lane] = valid ? __ffs(rpeers) - 1 : -1;
+                s_q[lane] = in ? __ldg(drow + (size_t)t * k + lane) : -1;
             }
-            if (lane < KMAX && lane >= __popc(b)) s_row[lane] = -1;
         }
         __syncthreads();
         int rr[KMAX];
-        float wj[KMAX];
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            rr[j] = s_row[j];
-            wj[j] = s_w[j];
-        }
+        for (int j = 0; j < KMAX; ++j) rr[j] = s_row[j];
         for (int v = threadIdx.x; v < nvec; v += kThreads) {
             uint4 val[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
                 if (rr[j] >= 0) val[j] = __ldg(y + (size_t)rr[j] * nvec + v);
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (rr[j] >= 0) acc8(acc, wj[j], val[j]);
-            partial[(size_t)q * nvec + v] = pack8(acc);
+            for (int j = 0; j < KMAX; ++j) {
+                const int q = s_q[j];  // block-uniform: the bookkeeping stays in shared memory
+                if (q < 0) continue;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = j; i < KMAX; ++i)
+                    if (s_lead[i] == j) acc8(acc, s_w[i], val[i]);
+                partial[(size_t)q * nvec + v] = pack8(acc);
+            }
         }
         __syncthreads();
     }
@@ -158,37 +167,32 @@ cudaError_t launch_expand(const DedupArgs& a, const void* dx, const float* dscal
                           int max_rows, int sm_count, cudaStream_t s)
 {
     if (max_rows <= 0) return cudaSuccess;
-    const int blocks = max_rows < sm_count * 16 ? max_rows : sm_count * 16;
+    (void)sm_count;
+    const int blocks = max_rows;  // one CTA per possible dedup row (the rest exit)
     return launch_pdl(expand_kernel, dim3(blocks), dim3(kThreads), s, a, (const uint4*)dx, dscale,
                       row_bytes / 16, dscale ? nblk : 0, (uint4*)recv_x, recv_scale, recv_src);
 }
 
-cudaError_t launch_combine_partial(const DedupArgs& a, const float* w, const void* y, int H,
-                                   void* partial, int max_rows, int sm_count, cudaStream_t s)
+cudaError_t launch_combine_partial(const RowArgs& ex, const int32_t* row, const int32_t* drow,
+                                   int L, const float* w, const void* y, int H, void* partial,
+                                   int sm_count, cudaStream_t s)
 {
-    if (max_rows <= 0) return cudaSuccess;
-    const int blocks = max_rows < sm_count * 16 ? max_rows : sm_count * 16;
-    const int per = a.ex.k < a.L ? a.ex.k : a.L;  // experts of a token on one rank
+    const int T = ex.T, k = ex.k;
+    if (T <= 0) return cudaSuccess;
+    const int blocks = T < sm_count * 16 ? T : sm_count * 16;
     const uint4* yy = (const uint4*)y;
     uint4* pp = (uint4*)partial;
     const int nvec = H / 8;
-    if (per <= 1)
-        return launch_pdl(combine_partial_kernel<1>, dim3(blocks), dim3(kThreads), s, a, w, yy,
-                          nvec, pp);
-    if (per <= 2)
-        return launch_pdl(combine_partial_kernel<2>, dim3(blocks), dim3(kThreads), s, a, w, yy,
-                          nvec, pp);
-    if (per <= 4)
-        return launch_pdl(combine_partial_kernel<4>, dim3(blocks), dim3(kThreads), s, a, w, yy,
-                          nvec, pp);
-    if (per <= 8)
-        return launch_pdl(combine_partial_kernel<8>, dim3(blocks), dim3(kThreads), s, a, w, yy,
-                          nvec, pp);
-    if (per <= 16)
-        return launch_pdl(combine_partial_kernel<16>, dim3(blocks), dim3(kThreads), s, a, w, yy,
-                          nvec, pp);
-    return launch_pdl(combine_partial_kernel<32>, dim3(blocks), dim3(kThreads), s, a, w, yy, nvec,
-                      pp);
+#define MOEEP_PARTIAL(KM)                                                                   \
+    return launch_pdl(combine_partial_kernel<KM>, dim3(blocks), dim3(kThreads), s, ex.idx, row, \
+                      drow, w, T, k, ex.E, L, yy, nvec, pp)
+    if (k <= 1) MOEEP_PARTIAL(1);
+    if (k <= 2) MOEEP_PARTIAL(2);
+    if (k <= 4) MOEEP_PARTIAL(4);
+    if (k <= 8) MOEEP_PARTIAL(8);
+    if (k <= 16) MOEEP_PARTIAL(16);
+    MOEEP_PARTIAL(32);
+#undef MOEEP_PARTIAL
 }
 
 }  // namespace moeep

@@ -28,6 +28,16 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kThreads = 128;
 constexpr int kUnroll = 8;  // 16-byte vectors per thread per pass (H <= 8192 in one pass)
 
+// CTA 0: the caller's copies of the column counts and offsets.
+__device__ __forceinline__ void copy_counts(const RowArgs& ra, const int32_t* cnt,
+                                            int32_t* recv_cnt)
+{
+    for (int c = threadIdx.x; c <= ra.ncols; c += blockDim.x) {
+        if (recv_cnt && c < ra.ncols) recv_cnt[c] = cnt[c];
+        if (ra.off_out) ra.off_out[c] = ra.off[c];
+    }
+}
+
 // Warp 0: rows of token t into s_row, the row map and recv_src.
 __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* row,
                                             int32_t* recv_src, int* s_row)
@@ -52,8 +62,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0 && recv_cnt)
-        for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
     for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {
         const uint4* xt = x + (size_t)t * nvec;
         // the pass loop is uniform across the CTA (it holds a barrier)
@@ -91,8 +100,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0 && recv_cnt)
-        for (int e = threadIdx.x; e < ra.E; e += blockDim.x) recv_cnt[e] = cnt[e];
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
     const int lane = threadIdx.x & 31;
     const int nblk = nvec / 16;
     for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {

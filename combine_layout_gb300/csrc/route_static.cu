@@ -151,6 +151,7 @@ extern "C" MOE_EP_API int moe_ep_route_layout_static(
     ra.G = 1;
     ra.ncols = experts;
     ra.mask = nullptr;
+    ra.off_out = nullptr;
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
