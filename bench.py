@@ -44,6 +44,8 @@ METRIC = "dispatch+combine tokens/s at T=4096,H=7168,top-8; achieved HBM GB/s vs
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNELS_PER_STEP = 3  # route (+ layout), dispatch (+ row map), combine
+# --path dedup: route, rank layout, dedup dispatch, expand, row map, partials, combine
+KERNELS_PER_STEP_DEDUP = 7
 
 
 # ------------------------------------------------------------------ helpers
@@ -58,6 +60,20 @@ def algorithmic_bytes(w: synth.Workload) -> dict:
     combine = T * k * (2 * H + 4 + 4) + T * 2 * H
     route = T * E * 4 + T * k * 8 + ((T + 31) // 32) * E * 4
     return {"dispatch": dispatch, "combine": combine, "route": route}
+
+
+def algorithmic_bytes_dedup(w: synth.Workload, nd: int) -> dict:
+    """Per-rank dedup path, nd dedup rows: dispatch = one copy per (token,
+    rank) (payload, scales, token, mask) + the receiver's expansion into the
+    T*k expert rows; combine = the k gathered rows and weights read, one BF16
+    partial per dedup row written and read back, the token written."""
+    T, H, k = w.T, w.H, w.k
+    payload = H if w.fp8 else 2 * H
+    scales = (H // 128) * 4 if w.fp8 else 0
+    dispatch = (T * (2 * H + k * 4) + nd * (payload + scales + 8)
+                + nd * (payload + scales + 8) + T * k * (payload + scales + 4))
+    combine = T * k * (2 * H + 4 + 4) + 2 * nd * 2 * H + T * 2 * H
+    return {"dispatch": dispatch, "combine": combine}
 
 
 def measured_peak_gbs():
@@ -203,14 +219,25 @@ def run_gpu(args) -> dict | None:
     # the step's GPU work instead of splitting it.
     bs = BoundStep(p, scores, x, y, w.T, w.G, w.kg, 0, w.weight_mode, stream)
 
+    dedup = args.path == "dedup"
+    if dedup and not ht:
+        raise SystemExit("--path dedup needs an HT workload")
+
     def step(ev=None):
         bs.route()
         if ev is not None:
             ev[0].record(stream)
-        bs.dispatch()
+        if dedup:
+            p.dispatch_dedup(x, stream)
+            p.expand(stream)
+        else:
+            bs.dispatch()
         if ev is not None:
             ev[1].record(stream)
-        bs.combine()
+        if dedup:
+            p.combine_dedup(y, stream=stream)
+        else:
+            bs.combine()
         if ev is not None:
             ev[2].record(stream)
         if ht:
@@ -258,6 +285,15 @@ def run_gpu(args) -> dict | None:
     barrier()
     d_ms = [e[0].elapsed_time(e[1]) for e in evs]
     c_ms = [e[1].elapsed_time(e[2]) for e in evs]
+
+    nd = int(p.rank_off[-1].item()) if dedup else None
+    if dedup:                       # the direct path's end-to-end leg only
+        p.close()
+        if world > 1:
+            dist.destroy_process_group()
+        if rank != 0:
+            return None
+        return _line(args, w, world, ms, d_ms, c_ms, clk, p.rows, ht, None, None, nd)
 
     # --- end to end: every step copies its inputs (scores, tokens) from pinned
     # host memory and its combined output back.  Inputs and outputs are double
@@ -323,17 +359,24 @@ def run_gpu(args) -> dict | None:
         dist.destroy_process_group()
     if rank != 0:
         return None
+    e2e = {"value": whole_job_rate(w.T, world, e2e_steps, e2e_ms), "unit": UNIT,
+           "h2d_bytes_per_step": scores_h.numel() * 4 + x_h.numel() * 2,
+           "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": e2e_steps,
+           "overlap": "double-buffered inputs/outputs; copies on their own streams"}
+    return _line(args, w, world, ms, d_ms, c_ms, clk, p.rows, ht, e2e, rt, None)
 
-    tokens = w.T * world
+
+def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
+    """The JSON line of one timed run (nd: dedup rows of the dedup path, else None)."""
     value = whole_job_rate(w.T, world, args.steps, ms)
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w) if nd is None else algorithmic_bytes_dedup(w, nd)
     d_avg = statistics.mean(d_ms)
     c_avg = statistics.mean(c_ms)
     dom = "dispatch" if d_avg >= c_avg else "combine"
     dom_ms = d_avg if dom == "dispatch" else c_avg
     peak, peak_src = measured_peak_gbs()
     achieved = ab[dom] / (dom_ms / 1e3) / 1e9
-    traffic = profiled_traffic(dom, w.name)
+    traffic = profiled_traffic(dom, w.name) if nd is None else None
     line = {
         "metric": METRIC,
         "value": value,
@@ -352,8 +395,9 @@ def run_gpu(args) -> dict | None:
                    "nodes": w.G, "max_nodes": w.kg,
                    "mode": "HT" if ht else "LL", "fp8": w.fp8,
                    "l2": "inputs larger than L2: each step writes and reads a "
-                         f"{p.rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer",
-                   "parallelism": f"replicas x{world} (logical ranks inside each GPU)"},
+                         f"{rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer",
+                   "parallelism": f"replicas x{world} (logical ranks inside each GPU)",
+                   **({} if nd is None else {"path": "dedup", "dedup_rows": nd})},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -368,11 +412,8 @@ def run_gpu(args) -> dict | None:
             "route_layout_query_us_by_difference": (ms / args.steps - d_avg - c_avg) * 1e3,
             "dispatch_combine_tokens_per_s": w.T / ((d_avg + c_avg) / 1e3),
         },
-        "e2e": {"value": whole_job_rate(w.T, world, e2e_steps, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": scores_h.numel() * 4 + x_h.numel() * 2,
-                "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": e2e_steps,
-                "overlap": "double-buffered inputs/outputs; copies on their own streams"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": e2e,
+        "gpu_launches": (KERNELS_PER_STEP if nd is None else KERNELS_PER_STEP_DEDUP) * args.steps,
         "clocks": clk,
         "round_trip_max_abs_err": rt,
     }
@@ -449,6 +490,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="direct", choices=["direct", "dedup"],
+                    help="dedup: one copy per (token, rank), expanded on the receiver, "
+                         "two-stage combine (HT workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
