@@ -551,7 +551,8 @@ int moe_ep_dequant(moe_ep_handle_t h, const void* recv_q, const float* recv_scal
         ((uintptr_t)recv_scale & 3u))
         return MOE_EP_ERR_INVALID;
     return cuda_status(launch_dequant(h->cnt, h->off, g->E, g->S, g->mode, g->H,
-                                      (const uint8_t*)recv_q, recv_scale, y, g->sm_count,
+                                      (const uint8_t*)recv_q, recv_scale, y,
+                                      (int64_t)h->T * h->k, g->sm_count, g->err_dev,
                                       (cudaStream_t)stream));
 }
 
@@ -790,6 +791,7 @@ int moe_ep_get_device_errors(moe_ep_group_t g, uint32_t* bits)
     uint32_t b = 0;
     if (g->err_host[kErrRange]) b |= MOE_EP_DEVERR_EXPERT_RANGE;
     if (g->err_host[kErrDuplicate]) b |= MOE_EP_DEVERR_DUPLICATE;
+    if (g->err_host[kErrTimeout]) b |= MOE_EP_DEVERR_TIMEOUT;
     *bits = b;
     return MOE_EP_OK;
 }

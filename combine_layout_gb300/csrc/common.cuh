@@ -21,6 +21,7 @@ constexpr int kMaxExperts = 512;
 constexpr int kErrSlots = 4;
 constexpr int kErrRange = 0;
 constexpr int kErrDuplicate = 1;
+constexpr int kErrTimeout = 2;  // a bounded wait inside a kernel gave up
 
 // Every kernel of the library is launched with programmatic stream
 // serialization: its CTAs may become resident while the kernel before it on
@@ -31,13 +32,13 @@ constexpr int kErrDuplicate = 1;
 // dependents as soon as every CTA has written its tile (the grid's last CTA
 // then finishes the layout while the next kernel's CTAs are being placed).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
-                       Args... args)
+cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -45,6 +46,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                       Args... args)
+{
+    return launch_pdl_smem(kernel, grid, block, 0, s, args...);
 }
 
 #ifdef __CUDACC__
@@ -158,9 +166,12 @@ cudaError_t launch_node_layout(const NodeArgs& a, const LayoutArgs& la, unsigned
 
 // Receive-side dequantisation of the rows the layout defines:
 // y = bf16_rn(float(q) * scale) (fp32 product).
+// err: the group's device-error word (kErrTimeout is latched there if a
+// bounded wait of the TMA-staged variant gives up).
+// max_rows: an upper bound of the defined rows (sizes the grid).
 cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S, int mode, int H,
-                           const uint8_t* q, const float* scale, void* y, int sm_count,
-                           cudaStream_t s);
+                           const uint8_t* q, const float* scale, void* y, int64_t max_rows,
+                           int sm_count, unsigned* err, cudaStream_t s);
 
 // Per-rank dedup, receiver side: copy every dedup row to the HT rows of its
 // local experts (row_bytes per row, nblk scales per row when dscale is set),

@@ -30,17 +30,11 @@ __device__ __forceinline__ uint32_t dequant_pair(uint16_t two_fp8, float s)
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-__global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __restrict__ cnt,
-                                                           const int32_t* __restrict__ off, int E,
-                                                           int S, int mode, int H,
-                                                           const uint4* __restrict__ q,
-                                                           const float* __restrict__ scale,
-                                                           uint4* __restrict__ y)
+// Exclusive prefix of the actual counts into s_pre[0..E] (s_pre[E] = the
+// number of defined rows); all threads of the CTA.
+__device__ __forceinline__ void count_prefix(const int32_t* __restrict__ cnt, int E, int* s_pre,
+                                             int* s_part)
 {
-    griddep_wait();
-    __shared__ int s_pre[kMaxExperts + 1];
-    __shared__ int s_part[kThreads];
-    // exclusive prefix of the actual counts
     const int tid = threadIdx.x;
     const int per = (E + kThreads - 1) / kThreads;
     const int lo = min(tid * per, E), hi = min(lo + per, E);
@@ -64,20 +58,38 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
         run += __ldg(cnt + e);
     }
     __syncthreads();
+}
 
+// Row of the i-th defined row: expert e = the last e with s_pre[e] <= i.
+__device__ __forceinline__ int defined_row(const int* s_pre, int E, int i,
+                                           const int32_t* __restrict__ off, int S, int mode)
+{
+    int a = 0, b = E;
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (s_pre[m] <= i) a = m; else b = m;
+    }
+    return (mode == MOE_EP_HT ? __ldg(off + a) : a * S) + (i - s_pre[a]);
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __restrict__ cnt,
+                                                           const int32_t* __restrict__ off, int E,
+                                                           int S, int mode, int H,
+                                                           const uint4* __restrict__ q,
+                                                           const float* __restrict__ scale,
+                                                           uint4* __restrict__ y)
+{
+    griddep_wait();
+    __shared__ int s_pre[kMaxExperts + 1];
+    __shared__ int s_part[kThreads];
+    const int tid = threadIdx.x;
+    count_prefix(cnt, E, s_pre, s_part);
     const int total = s_pre[E];
     const int lane = tid & 31, wpc = kThreads / 32;
     const int nvq = H / 16;   // 16-byte vectors of FP8 per row
     const int nbk = H / 128;  // scales per row
     for (int i = blockIdx.x * wpc + (tid >> 5); i < total; i += gridDim.x * wpc) {
-        // expert of defined row i: the last e with s_pre[e] <= i
-        int a = 0, b = E;
-        while (b - a > 1) {
-            const int m = (a + b) >> 1;
-            if (s_pre[m] <= i) a = m; else b = m;
-        }
-        const int e = a;
-        const int row = (mode == MOE_EP_HT ? __ldg(off + e) : e * S) + (i - s_pre[e]);
+        const int row = defined_row(s_pre, E, i, off, S, mode);
         const uint4* qr = q + (size_t)row * nvq;
         const float* sr = scale + (size_t)row * nbk;
         uint4* yr = y + (size_t)row * (H / 8);
@@ -111,14 +123,161 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
     }
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged variant (H % 512 == 0: a row's scales are a whole number of
+// 16-byte units).  Every CTA keeps kStages rows in flight in shared memory:
+// one thread issues a bulk copy (cp.async.bulk, completion counted on the
+// stage's mbarrier) of each defined row's FP8 values and scales; all threads
+// convert the staged row and store bf16 with 16-byte stores.  The copies hold
+// no registers, so far more bytes are in flight per SM than with loads into
+// registers.  Every mbarrier wait is bounded: a wait that gives up latches
+// kErrTimeout, the CTA stops converting, waits (bounded) for the copies it
+// still has in flight and returns.
+
+constexpr int kStages = 8;
+constexpr uint32_t kWaitPolls = 1u << 22;  // try_wait polls before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t it = 0; it < kWaitPolls; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_tma_kernel(const int32_t* __restrict__ cnt,
+                                                               const int32_t* __restrict__ off,
+                                                               int E, int S, int mode, int H,
+                                                               const uint8_t* __restrict__ q,
+                                                               const float* __restrict__ scale,
+                                                               uint4* __restrict__ y,
+                                                               unsigned* err)
+{
+    griddep_wait();
+    extern __shared__ __align__(128) unsigned char s_buf[];  // kStages x (H + H/32) bytes
+    __shared__ __align__(8) unsigned long long s_bar[kStages];
+    __shared__ int s_row[kStages];
+    __shared__ int s_pre[kMaxExperts + 1];
+    __shared__ int s_part[kThreads];
+    __shared__ int s_fail;
+    const int tid = threadIdx.x;
+    count_prefix(cnt, E, s_pre, s_part);
+    const int total = s_pre[E];
+    const int first = blockIdx.x;
+    const int mine = first < total ? (total - 1 - first) / (int)gridDim.x + 1 : 0;
+    const uint32_t qbytes = (uint32_t)H, sbytes = (uint32_t)(H / 32), stage = qbytes + sbytes;
+    const int nvq = H / 16, nbk = H / 128;
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(smem_u32(&s_bar[st]));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_fail = 0;
+    }
+    __syncthreads();
+    // thread 0: stage n's row into buffer n % kStages
+    auto issue = [&](int n) {
+        const int st = n % kStages;
+        const int row = defined_row(s_pre, E, first + n * (int)gridDim.x, off, S, mode);
+        s_row[st] = row;
+        const uint32_t bar = smem_u32(&s_bar[st]);
+        unsigned char* dst = s_buf + (size_t)st * stage;
+        mbar_expect_tx(bar, stage);
+        bulk_load(smem_u32(dst), q + (size_t)row * H, qbytes, bar);
+        bulk_load(smem_u32(dst + qbytes), scale + (size_t)row * nbk, sbytes, bar);
+    };
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < min(kStages, mine); ++issued) issue(issued);
+    int n = 0;
+    for (; n < mine; ++n) {
+        const int st = n % kStages;
+        const bool ok = mbar_wait(smem_u32(&s_bar[st]), (uint32_t)((n / kStages) & 1));
+        if (ok) {
+            const uint4* qs = reinterpret_cast<const uint4*>(s_buf + (size_t)st * stage);
+            const float* ss = reinterpret_cast<const float*>(s_buf + (size_t)st * stage + qbytes);
+            uint4* yr = y + (size_t)s_row[st] * (H / 8);
+            for (int v = tid; v < nvq; v += kThreads) {
+                const uint4 w = qs[v];
+                const float sc = ss[v >> 3];
+                const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    o[2 * c] = dequant_pair((uint16_t)(x[c] & 0xffffu), sc);
+                    o[2 * c + 1] = dequant_pair((uint16_t)(x[c] >> 16), sc);
+                }
+                yr[2 * v] = make_uint4(o[0], o[1], o[2], o[3]);
+                yr[2 * v + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        } else {
+            s_fail = 1;
+        }
+        __syncthreads();  // the stage is free again (and s_fail is seen by all)
+        if (s_fail) break;
+        if (tid == 0 && issued < mine) issue(issued++);
+    }
+    if (s_fail && tid == 0) {
+        err[kErrTimeout] = 1u;
+        // the copies still in flight into this CTA's shared memory: wait for
+        // them (bounded) before the CTA exits
+        for (int m = n; m < issued; ++m)
+            mbar_wait(smem_u32(&s_bar[m % kStages]), (uint32_t)((m / kStages) & 1));
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S, int mode, int H,
-                           const uint8_t* q, const float* scale, void* y, int sm_count,
-                           cudaStream_t s)
+                           const uint8_t* q, const float* scale, void* y, int64_t max_rows,
+                           int sm_count, unsigned* err, cudaStream_t s)
 {
-    return launch_pdl(dequant_kernel, dim3(sm_count * 8), dim3(kThreads), s, cnt, off, E, S, mode, H,
-                      (const uint4*)q, scale, (uint4*)y);
+    const size_t stage = (size_t)H + H / 32;
+    const size_t smem = kStages * stage;
+    const int per_sm = smem <= 96 * 1024 ? 2 : 1;
+    // staging pays once every CTA has rings of rows to stream; a small batch
+    // (LL decode) is latency-bound and does better with a warp per row on
+    // every SM, leaving shared memory to kernels of other streams
+    const bool tma = H % 512 == 0 && ((uintptr_t)q & 15u) == 0 && ((uintptr_t)scale & 15u) == 0 &&
+                     smem <= 160 * 1024 && max_rows >= (int64_t)kStages * sm_count * per_sm;
+    if (!tma)
+        return launch_pdl(dequant_kernel, dim3(sm_count * 8), dim3(kThreads), s, cnt, off, E, S,
+                          mode, H, (const uint4*)q, scale, (uint4*)y);
+    cudaError_t e = cudaFuncSetAttribute(dequant_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_smem(dequant_tma_kernel, dim3(sm_count * per_sm), dim3(kThreads), smem, s,
+                           cnt, off, E, S, mode, H, q, scale, (uint4*)y, err);
 }
 
 }  // namespace moeep

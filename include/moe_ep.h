@@ -66,6 +66,9 @@ typedef enum {
 /* Bits of the device-error word. */
 #define MOE_EP_DEVERR_EXPERT_RANGE 1u /* a topk_idx entry outside [-1, experts) */
 #define MOE_EP_DEVERR_DUPLICATE 2u    /* an expert repeated within one token */
+#define MOE_EP_DEVERR_TIMEOUT 4u      /* a bounded wait inside a kernel gave up (the
+                                         kernel latched it, skipped the rest of its
+                                         work and returned; outputs are incomplete) */
 
 typedef enum {
     MOE_EP_W_SOFTMAX_TOPK = 0,   /* w_j = softmax over the k selected scores */

@@ -63,7 +63,24 @@ def test_aligned_layout_and_round_trip(name, T, align):
                                           ("ll_decode", 128, 1), ("ll_decode", 45, 1),
                                           ("ht_prefill_fp8", 4096, 1)])
 def test_dequant_matches_oracle(name, T, align):
-    w = synth.WORKLOADS[name].with_tokens(T, slots=synth.WORKLOADS[name].slots or None)
+    _dequant_check(synth.WORKLOADS[name].with_tokens(T, slots=synth.WORKLOADS[name].slots or None),
+                   align)
+
+
+@pytest.mark.parametrize("H,T,align", [(640, 300, 1), (640, 800, 16), (512, 300, 1),
+                                       (512, 800, 1), (1536, 800, 8)])
+def test_dequant_hidden_sizes(H, T, align):
+    """H % 512 == 0 with at least 8 rows per CTA of two per SM (T*k >= 2432
+    here) takes the TMA-staged kernel (rows staged in shared memory by bulk
+    copies); other widths and small batches the register-path kernel.  Both
+    against the oracle."""
+    w = synth.Workload("narrow", T=T, H=H, E=32, R=8, k=4, mode=synth.MODE_HT, fp8=True,
+                       scores="uniform_bias", weight_mode=synth.W_SCORE_NORM, seed=3)
+    _dequant_check(w, align)
+
+
+def _dequant_check(w, align):
+    T = w.T
     inp = synth.make_inputs(w)
     p = _pipe(w, align, fp8=True)
     p.route(torch.from_numpy(inp["scores"]).to(DEV), T, w.G, w.kg, 0, w.weight_mode)
