@@ -91,8 +91,69 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
     }
 }
 
-// Thread i handles vectors i + u*128: a half-warp (16 lanes x 8 elements)
-// covers exactly one 128-element block.
+// FP8 e4m3 of one 16-byte vector of eight bf16 values; a half-warp (16 lanes
+// x 8 elements) holds one 128-element block.  All 32 lanes must call it
+// (the block maximum is reduced with shuffles).  *scale receives the block's
+// scale amax / 448 (1 when the block is all zeros).
+__device__ __forceinline__ uint2 quant8(const uint4& raw, float* scale_out)
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    // Quotients rounded to nearest (IEEE) by Markstein's method: with r =
+    // RN(1/d), q0 = RN(a*r) is within 1 ulp of a/d and RN(q0 + (a - q0*d)*r)
+    // is exactly RN(a/d), the remainder being exact in one fma -- provided
+    // nothing overflows or underflows, which 2^-80 <= amax <= 2^100
+    // guarantees both for the scale amax / 448 and for every element quotient
+    // whose e4m3 code depends on its low bits (smaller quotients all give the
+    // code 0).  Other blocks divide directly.
+    const bool fast = amax >= 0x1p-80f && amax <= 0x1p+100f;  // uniform per block
+    float scale, rs;
+    if (fast) {
+        constexpr float kR448 = 0x1.24924ap-9f;  // RN(1/448)
+        const float s0 = __fmul_rn(amax, kR448);
+        scale = __fmaf_rn(__fmaf_rn(-s0, 448.f, amax), kR448, s0);
+        rs = __frcp_rn(scale);
+    } else {
+        scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        rs = 0.f;
+    }
+    float qt[8];
+    if (fast) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q0 = __fmul_rn(f[i], rs);
+            const float rem = __fmaf_rn(-q0, scale, f[i]);
+            qt[i] = (f[i] == 0.f) ? f[i] : __fmaf_rn(rem, rs, q0);  // keep the sign of 0
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qt[i] = __fdiv_rn(f[i], scale);
+    }
+    uint32_t packed[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(qt[4 * h + 0], qt[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(qt[4 * h + 2], qt[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
+        packed[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    *scale_out = scale;
+    return make_uint2(packed[0], packed[1]);
+}
+
+// General FP8 dispatch (any H, multiple of 128): thread i handles vectors
+// i + u*128 of each pass of kUnroll*128 vectors.
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
@@ -118,53 +179,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
             uint2 q[kUnroll];
             float sc[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-                float f[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    f[2 * i] = __uint_as_float(w[i] << 16);
-                    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-                }
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-                const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
-                // x / scale rounded to nearest (IEEE), by Markstein's method: with
-                // r = RN(1/scale), q0 = RN(x*r) is within 1 ulp of x/scale and
-                // RN(q0 + (x - q0*scale)*r) is exactly RN(x/scale), the remainder
-                // being exact in one fma -- provided nothing overflows or
-                // underflows, which 2^-80 <= amax <= 2^100 guarantees for every
-                // quotient whose e4m3 code depends on its low bits (smaller
-                // quotients all give the code 0).  Other blocks divide directly.
-                const bool fast = amax >= 0x1p-80f && amax <= 0x1p+100f;  // uniform per block
-                const float rs = fast ? __frcp_rn(scale) : 0.f;
-                float qt[8];
-                if (fast) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float q0 = __fmul_rn(f[i], rs);
-                        const float rem = __fmaf_rn(-q0, scale, f[i]);
-                        qt[i] = (f[i] == 0.f) ? f[i] : __fmaf_rn(rem, rs, q0);  // keep the sign of 0
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) qt[i] = __fdiv_rn(f[i], scale);
-                }
-                uint32_t packed[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                        make_float2(qt[4 * h + 0], qt[4 * h + 1]), __NV_SATFINITE, __NV_E4M3);
-                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                        make_float2(qt[4 * h + 2], qt[4 * h + 3]), __NV_SATFINITE, __NV_E4M3);
-                    packed[h] = (uint32_t)lo | ((uint32_t)hi << 16);
-                }
-                q[u] = make_uint2(packed[0], packed[1]);
-                sc[u] = scale;
-            }
+            for (int u = 0; u < kUnroll; ++u) q[u] = quant8(raw[u], &sc[u]);
             if (pass == 0) place_token(ra, t, row, recv_src, s_row);
             __syncthreads();
             for (int j = 0; j < ra.k; ++j) {
@@ -186,6 +201,47 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     }
 }
 
+// FP8 dispatch for rows of exactly NV * 128 vectors (H = 1024 * NV): no
+// bounds checks, and each token's NV * 8 scales go through shared memory so
+// every row's scales are one coalesced store.
+template <int NV>
+__global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
+    RowArgs ra, const uint4* __restrict__ x, int32_t* __restrict__ row,
+    uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
+    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
+{
+    constexpr int nvec = NV * kThreads, nblk = nvec / 16;
+    griddep_wait();
+    __shared__ int s_row[kMaxTopk];
+    __shared__ float s_sc[nblk];
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
+    const int tid = threadIdx.x;
+    for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {
+        const uint4* xt = x + (size_t)t * nvec;
+        uint4 raw[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) raw[u] = __ldg(xt + tid + u * kThreads);
+        uint2 q[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            float sc;
+            q[u] = quant8(raw[u], &sc);
+            if ((tid & 15) == 0) s_sc[(tid + u * kThreads) >> 4] = sc;
+        }
+        place_token(ra, t, row, recv_src, s_row);
+        __syncthreads();
+        for (int j = 0; j < ra.k; ++j) {
+            const int r = s_row[j];
+            if (r < 0) continue;
+            uint2* dst = recv_q + (size_t)r * nvec;
+#pragma unroll
+            for (int u = 0; u < NV; ++u) dst[tid + u * kThreads] = q[u];
+            if (tid < nblk) recv_scale[(size_t)r * nblk + tid] = s_sc[tid];
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
@@ -195,6 +251,24 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
     (void)sm_count;
     const int nvec = H / 8;
     const int blocks = ra.T < 1 ? 1 : ra.T;
+    if (fp8 && nvec % kThreads == 0 && nvec / kThreads <= 8) {
+#define MOEEP_FP8_FIT(N)                                                                         \
+    case N:                                                                                      \
+        return launch_pdl(dispatch_fp8_fit_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,      \
+                          (const uint4*)x, row, (uint2*)recv_x, recv_scale, recv_src, cnt,      \
+                          recv_cnt);
+        switch (nvec / kThreads) {
+            MOEEP_FP8_FIT(1)
+            MOEEP_FP8_FIT(2)
+            MOEEP_FP8_FIT(3)
+            MOEEP_FP8_FIT(4)
+            MOEEP_FP8_FIT(5)
+            MOEEP_FP8_FIT(6)
+            MOEEP_FP8_FIT(7)
+            MOEEP_FP8_FIT(8)
+        }
+#undef MOEEP_FP8_FIT
+    }
     if (fp8)
         return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
                           (const uint4*)x, nvec, row, (uint2*)recv_x, recv_scale, recv_src, cnt,

@@ -225,3 +225,26 @@ def _fp8_bytes_match_oracle(xb):
         bad = np.nonzero(q[t] != qo)[0]
         assert bad.size == 0, (t, bad[:4], q[t][bad[:4]], qo[bad[:4]])
     p.close()
+
+
+def test_fp8_scale_for_every_bf16_block_maximum():
+    """The block maximum is always a bf16 value: every positive finite one
+    (0x0001 .. 0x7f7f) is some block's maximum here, so the scale amax / 448
+    (Markstein's method inside 2^-80 .. 2^100, IEEE division outside) is
+    compared with the oracle's fp32 division for every value it can take, and
+    the bytes of the block's other elements with it."""
+    rng = np.random.default_rng(23)
+    amax_bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    H = 7168
+    nblk = H // 128
+    T = -(-amax_bits.size // nblk)
+    amax = np.ones(T * nblk, np.uint16) * 0x3F80          # padding blocks: amax 1.0
+    amax[: amax_bits.size] = amax_bits
+    af = synth.bf16_bits_to_f32(amax).astype(np.float64)
+    blocks = rng.uniform(-1.0, 1.0, (T * nblk, 128)) * af[:, None]
+    xb = synth.f32_to_bf16_bits(blocks.astype(np.float32))
+    big = np.abs(synth.bf16_bits_to_f32(xb)) > synth.bf16_bits_to_f32(amax)[:, None]
+    xb = np.where(big, amax[:, None], xb)                 # rounding must not exceed amax
+    pos = rng.integers(0, 128, T * nblk)
+    xb[np.arange(T * nblk), pos] = amax                   # the maximum itself
+    _fp8_bytes_match_oracle(xb.reshape(T, H).astype(np.uint16))
