@@ -40,19 +40,20 @@ __device__ __forceinline__ void count_prefix(const int32_t* __restrict__ cnt, in
     const int lo = min(tid * per, E), hi = min(lo + per, E);
     int sum = 0;
     for (int e = lo; e < hi; ++e) sum += __ldg(cnt + e);
-    s_part[tid] = sum;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int v = s_part[i];
-            s_part[i] = run;
-            run += v;
-        }
-        s_pre[E] = run;
+    // block-wide exclusive scan of the per-thread sums: warp scans, then the
+    // warp totals (s_part holds the kThreads / 32 totals)
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
+    if (lane == 31) s_part[warp] = incl;
     __syncthreads();
-    int run = s_part[tid];
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += s_part[w];
+    if (tid == kThreads - 1) s_pre[E] = run + sum;
     for (int e = lo; e < hi; ++e) {
         s_pre[e] = run;
         run += __ldg(cnt + e);
@@ -270,9 +271,13 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
     // every SM, leaving shared memory to kernels of other streams
     const bool tma = H % 512 == 0 && ((uintptr_t)q & 15u) == 0 && ((uintptr_t)scale & 15u) == 0 &&
                      smem <= 160 * 1024 && max_rows >= (int64_t)kStages * sm_count * per_sm;
-    if (!tma)
-        return launch_pdl(dequant_kernel, dim3(sm_count * 8), dim3(kThreads), s, cnt, off, E, S,
-                          mode, H, (const uint4*)q, scale, (uint4*)y);
+    if (!tma) {
+        // one warp per row: no more CTAs than the rows can keep busy
+        const int64_t want = (max_rows + kThreads / 32 - 1) / (kThreads / 32);
+        const int blocks = (int)(want < 1 ? 1 : (want < sm_count * 8 ? want : sm_count * 8));
+        return launch_pdl(dequant_kernel, dim3(blocks), dim3(kThreads), s, cnt, off, E, S, mode,
+                          H, (const uint4*)q, scale, (uint4*)y);
+    }
     cudaError_t e = cudaFuncSetAttribute(dequant_tma_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
