@@ -95,6 +95,10 @@ struct LayoutArgs {
     // parts and groups per part, experts per prefix thread, prefix threads,
     // threads that take part at all.
     int L, cols, parts, rg, per, nact, nwork;
+    // 1: the producers wrote only tile_word (a tile's word assembled from the
+    // bytes of several CTAs); the last CTA derives tile_cnt from the words
+    // and writes it.  Only with ntiles <= 32 (at most two groups).
+    int cnt_from_words = 0;
     // Optional publication of the counts to the host (mapped pinned memory,
     // device alias): off[E+1], rcnt[R], cnt[E], then the sequence number
     // `seq`, written last, after a system-scope fence.  nullptr: none.

@@ -88,6 +88,22 @@ inline LayoutArgs tail_planned(LayoutArgs a, int nthr)
     return a;
 }
 
+// Byte counts of group g of column col from the tile words (tiles past
+// ntiles count 0), stored to tile_cnt for the consumers.
+__device__ __forceinline__ uint4 counts_from_words(const LayoutArgs& a, int g, int col)
+{
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < kGroupTiles; ++j) {
+        const int tile = g * kGroupTiles + j;
+        const uint32_t w = tile < a.ntiles ? __ldcg(a.tile_word + (size_t)tile * a.E + col) : 0u;
+        c[j >> 2] |= (uint32_t)__popc(w) << (8 * (j & 3));
+    }
+    const uint4 v = make_uint4(c[0], c[1], c[2], c[3]);
+    reinterpret_cast<uint4*>(a.tile_cnt)[(size_t)g * a.E + col] = v;
+    return v;
+}
+
 // Padded size of an expert block of c rows.
 __device__ __forceinline__ int padded(int c, int align)
 {
@@ -143,7 +159,16 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
         const bool act = part < parts && col < E;
         int gs[kTailVec];
         int sum = 0;
-        if (act) {
+        if (act && a.cnt_from_words) {  // at most two groups, one run
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                gs[i] = 0;
+                if (g0 + i < g1)
+                    gs[i] = vec_byte_sum(counts_from_words(a, g0 + i, col),
+                                         ntiles - (g0 + i) * kGroupTiles);
+                sum += gs[i];
+            }
+        } else if (act) {
             for (int b = g0; b < g1; b += kTailVec) {
                 uint4 v[kTailVec];
 #pragma unroll

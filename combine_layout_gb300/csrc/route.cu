@@ -26,6 +26,9 @@ namespace moeep {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+// Batches up to this many tokens (32 tiles, two groups of byte counts) are
+// routed 8 tokens per CTA.
+constexpr int kSplitMaxTokens = 1024;
 
 __device__ __forceinline__ uint32_t score_key(float x)
 {
@@ -233,12 +236,17 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
     out_w = w;
 }
 
-template <int EPL, bool VEC, int MG>
-__global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict__ scores, int T,
-                                                     RouteParams p, int32_t* __restrict__ topk_idx,
-                                                     int32_t* __restrict__ idx_copy,
-                                                     float* __restrict__ topk_w, LayoutArgs la)
+// One warp per token.  TPC = 32: a CTA routes a whole 32-token tile and
+// writes its tile words and byte counts.  TPC = 8 (small batches): four CTAs
+// share a tile, each writing its own byte of every tile word (the bits of its
+// 8 tokens), so four times as many SMs do the selection work; the last CTA
+// then derives the byte counts from the words.
+template <int EPL, bool VEC, int MG, int TPC>
+__global__ void __launch_bounds__(TPC * 32, TPC == kTileTokens ? 1 : 2) route_kernel(
+    const float* __restrict__ scores, int T, RouteParams p, int32_t* __restrict__ topk_idx,
+    int32_t* __restrict__ idx_copy, float* __restrict__ topk_w, LayoutArgs la)
 {
+    constexpr int kParts = kTileTokens / TPC;
     griddep_wait();
     __shared__ uint32_t s_word[kMaxExperts];
     __shared__ int s_scratch[kTailSmemInts];
@@ -246,8 +254,9 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
     for (int e = tid; e < p.E; e += blockDim.x) s_word[e] = 0u;
     __syncthreads();
 
-    const int tile = blockIdx.x;
-    const int t = tile * kTileTokens + warp;
+    const int tile = blockIdx.x / kParts, part = blockIdx.x % kParts;
+    const int slot = part * TPC + warp;  // the token's bit in its tile word
+    const int t = tile * kTileTokens + slot;
     if (t < T) {
         int e;
         float w;
@@ -257,14 +266,19 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(const float* __restrict_
             topk_idx[q] = e;
             idx_copy[q] = e;
             if (topk_w) topk_w[q] = w;
-            if (e >= 0) atomicOr(&s_word[e], 1u << warp);
+            if (e >= 0) atomicOr(&s_word[e], 1u << slot);
         }
     }
     __syncthreads();
     for (int e = tid; e < p.E; e += blockDim.x) {
         const uint32_t wd = s_word[e];
-        la.tile_word[(size_t)tile * p.E + e] = wd;
-        la.tile_cnt[tile_cnt_index(tile, e, p.E)] = (uint8_t)__popc(wd);
+        if constexpr (kParts == 1) {
+            la.tile_word[(size_t)tile * p.E + e] = wd;
+            la.tile_cnt[tile_cnt_index(tile, e, p.E)] = (uint8_t)__popc(wd);
+        } else {
+            reinterpret_cast<uint8_t*>(la.tile_word)[((size_t)tile * p.E + e) * 4 + part] =
+                (uint8_t)(wd >> (8 * part));
+        }
     }
     griddep_launch_dependents();
     finish_layout_if_last(la, s_scratch);
@@ -317,13 +331,24 @@ cudaError_t launch_route_mg(const float* scores, int T, const RouteParams& p, in
                      int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
-    const LayoutArgs lt = tail_planned(la, 1024);
     // the group list holds MG >= m keys (m = 1, 2: two; 3, 4: four)
-    if (!p.limit || p.m <= 2)
-        return launch_pdl(route_kernel<EPL, VEC, 2>, dim3(ntiles), dim3(1024), s, scores, T, p,
-                          topk_idx, idx_copy, topk_w, lt);
-    return launch_pdl(route_kernel<EPL, VEC, 4>, dim3(ntiles), dim3(1024), s, scores, T, p,
-                      topk_idx, idx_copy, topk_w, lt);
+    const bool mg2 = !p.limit || p.m <= 2;
+    if (T <= kSplitMaxTokens) {  // small batch: 8 tokens per CTA
+        LayoutArgs lt = tail_planned(la, 256);
+        lt.cnt_from_words = 1;
+        const dim3 grid(ntiles * (kTileTokens / 8)), block(256);
+        if (mg2)
+            return launch_pdl(route_kernel<EPL, VEC, 2, 8>, grid, block, s, scores, T, p,
+                              topk_idx, idx_copy, topk_w, lt);
+        return launch_pdl(route_kernel<EPL, VEC, 4, 8>, grid, block, s, scores, T, p, topk_idx,
+                          idx_copy, topk_w, lt);
+    }
+    const LayoutArgs lt = tail_planned(la, 1024);
+    if (mg2)
+        return launch_pdl(route_kernel<EPL, VEC, 2, kTileTokens>, dim3(ntiles), dim3(1024), s,
+                          scores, T, p, topk_idx, idx_copy, topk_w, lt);
+    return launch_pdl(route_kernel<EPL, VEC, 4, kTileTokens>, dim3(ntiles), dim3(1024), s,
+                      scores, T, p, topk_idx, idx_copy, topk_w, lt);
 }
 
 template <int EPL>
