@@ -23,21 +23,23 @@ constexpr int kThreads = 128;
 
 // Register budget per row count: enough CTAs per SM to keep the gathered rows
 // of many tokens in flight (k <= 8: 64 registers, 8 CTAs -- measured on the
-// bench shape 6.64 TB/s vs 6.29 TB/s with 5 CTAs; k <= 2: 32 registers).
+// bench shape 6.64 TB/s vs 6.29 TB/s with 5 CTAs; k <= 2: 40 registers).
 constexpr int combine_min_ctas(int kmax)
 {
-    return kmax <= 2 ? 16 : (kmax <= 4 ? 10 : (kmax <= 8 ? 8 : (kmax <= 16 ? 4 : 2)));
+    return kmax <= 2 ? 12 : (kmax <= 4 ? 10 : (kmax <= 8 ? 8 : (kmax <= 16 ? 4 : 2)));
 }
 
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kernel(
-    const uint4* __restrict__ y, int T, int k, int nvec, const int32_t* __restrict__ row,
-    const float* __restrict__ w, uint4* __restrict__ out)
+    const uint4* __restrict__ y, int T, int k, int nvec, int nsplit,
+    const int32_t* __restrict__ row, const float* __restrict__ w, uint4* __restrict__ out)
 {
     griddep_wait();
     __shared__ int s_row[KMAX];
     __shared__ float s_w[KMAX];
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const int chunk = nvec / nsplit;  // token t's slice sl: vectors [sl*chunk, (sl+1)*chunk)
+    for (int it = blockIdx.x; it < T * nsplit; it += gridDim.x) {
+        const int t = it / nsplit, sl = it - t * nsplit;
         if (threadIdx.x < k) {
             s_row[threadIdx.x] = row[(size_t)t * k + threadIdx.x];
             s_w[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
             r[j] = j < k ? s_row[j] : -1;
             wj[j] = j < k ? s_w[j] : 0.f;
         }
-        for (int v = threadIdx.x; v < nvec; v += kThreads) {
+        for (int v = sl * chunk + threadIdx.x; v < (sl + 1) * chunk; v += kThreads) {
             uint4 val[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
@@ -72,28 +74,23 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
 {
     if (T <= 0) return cudaSuccess;
     const int nvec = H / 8;
-    // one CTA per token, at most 16 per SM (grid-stride beyond: small tokens
-    // then amortise the CTA launch)
-    const int blocks = T < sm_count * 16 ? T : sm_count * 16;
+    // one CTA per token (or per token slice in small batches), at most 16
+    // per SM (grid-stride beyond: small tokens then amortise the CTA launch)
+    const int nsplit = (nvec % 16 == 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    const int items = T * nsplit;
+    const int blocks = items < sm_count * 16 ? items : sm_count * 16;
     const uint4* yy = (const uint4*)y;
     uint4* oo = (uint4*)out;
-    if (k <= 1)
-        return launch_pdl(combine_kernel<1>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
-                          row, w, oo);
-    if (k <= 2)
-        return launch_pdl(combine_kernel<2>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
-                          row, w, oo);
-    if (k <= 4)
-        return launch_pdl(combine_kernel<4>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
-                          row, w, oo);
-    if (k <= 8)
-        return launch_pdl(combine_kernel<8>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
-                          row, w, oo);
-    if (k <= 16)
-        return launch_pdl(combine_kernel<16>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,
-                          row, w, oo);
-    return launch_pdl(combine_kernel<32>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec, row, w,
-                      oo);
+#define MOEEP_COMBINE(KM)                                                                      \
+    return launch_pdl(combine_kernel<KM>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,     \
+                      nsplit, row, w, oo)
+    if (k <= 1) MOEEP_COMBINE(1);
+    if (k <= 2) MOEEP_COMBINE(2);
+    if (k <= 4) MOEEP_COMBINE(4);
+    if (k <= 8) MOEEP_COMBINE(8);
+    if (k <= 16) MOEEP_COMBINE(16);
+    MOEEP_COMBINE(32);
+#undef MOEEP_COMBINE
 }
 
 }  // namespace moeep

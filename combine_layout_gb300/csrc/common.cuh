@@ -156,6 +156,11 @@ cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* i
 // layout copy that comes without a dispatch).
 cudaError_t launch_rowmap(const RowArgs& ra, int32_t* row, int sm_count, cudaStream_t s);
 
+// Column slices per token for small batches: the smallest divisor of
+// `units` (equal slices of a row) that puts about two CTAs on every SM;
+// 1 when the tokens alone do.
+int slices_for(int T, int units, int sm_count);
+
 // Dispatch pack: x bf16 [T][H] -> receive rows (bf16 copy or FP8 + scales).
 // Also writes the row map and recv_src, and copies cnt into recv_cnt.
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,

@@ -38,9 +38,10 @@ __device__ __forceinline__ void copy_counts(const RowArgs& ra, const int32_t* cn
     }
 }
 
-// Warp 0: rows of token t into s_row, the row map and recv_src.
+// Warp 0: rows of token t into s_row; with `write` (the token's first slice)
+// also the row map, recv_src and the rank masks.
 __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* row,
-                                            int32_t* recv_src, int* s_row)
+                                            int32_t* recv_src, int* s_row, bool write)
 {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -48,33 +49,40 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
         const int r = token_pair_row(ra, t, lane, &m);
         if (lane < ra.k) {
             s_row[lane] = r;
-            row[(size_t)t * ra.k + lane] = r;
-            if (r >= 0 && recv_src) recv_src[r] = t;
-            if (r >= 0 && ra.mask) ra.mask[r] = m;
+            if (write) {
+                row[(size_t)t * ra.k + lane] = r;
+                if (r >= 0 && recv_src) recv_src[r] = t;
+                if (r >= 0 && ra.mask) ra.mask[r] = m;
+            }
         }
     }
 }
 
+// Work items: token t's slice sl of nsplit equal column slices (nsplit = 1
+// except for small batches, where several CTAs share a token's rows).
 __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
-    RowArgs ra, const uint4* __restrict__ x, int nvec, int32_t* __restrict__ row,
+    RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
     int32_t* __restrict__ recv_cnt)
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
     if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
-    for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {
+    const int chunk = nvec / nsplit;
+    for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
+        const int t = it / nsplit, sl = it - t * nsplit;
+        const int vb = sl * chunk, ve = vb + chunk;
         const uint4* xt = x + (size_t)t * nvec;
         // the pass loop is uniform across the CTA (it holds a barrier)
-        for (int pass = 0; pass < nvec; pass += kUnroll * kThreads) {
+        for (int pass = vb; pass < ve; pass += kUnroll * kThreads) {
             const int v0 = pass + threadIdx.x;
             uint4 buf[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int v = v0 + u * kThreads;
-                if (v < nvec) buf[u] = __ldg(xt + v);
+                if (v < ve) buf[u] = __ldg(xt + v);
             }
-            if (pass == 0) place_token(ra, t, row, recv_src, s_row);
+            if (pass == vb) place_token(ra, t, row, recv_src, s_row, sl == 0);
             __syncthreads();
             for (int j = 0; j < ra.k; ++j) {
                 const int r = s_row[j];
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const int v = v0 + u * kThreads;
-                    if (v < nvec) dst[v] = buf[u];
+                    if (v < ve) dst[v] = buf[u];
                 }
             }
         }
@@ -155,7 +163,7 @@ __device__ __forceinline__ uint2 quant8(const uint4& raw, float* scale_out)
 // General FP8 dispatch (any H, multiple of 128): thread i handles vectors
 // i + u*128 of each pass of kUnroll*128 vectors.
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
-    RowArgs ra, const uint4* __restrict__ x, int nvec, int32_t* __restrict__ row,
+    RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
     const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
 {
@@ -164,23 +172,26 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
     const int lane = threadIdx.x & 31;
     const int nblk = nvec / 16;
-    for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {
+    const int chunk = nvec / nsplit;  // a multiple of 16 vectors: whole 128-blocks
+    for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
+        const int t = it / nsplit, sl = it - t * nsplit;
+        const int vb = sl * chunk, ve = vb + chunk;
         const uint4* xt = x + (size_t)t * nvec;
         // the pass loop is uniform across the CTA (it holds a barrier and
-        // half-warp shuffles; lanes past the row end carry zeros)
-        for (int pass = 0; pass < nvec; pass += kUnroll * kThreads) {
+        // half-warp shuffles; lanes past the slice end carry zeros)
+        for (int pass = vb; pass < ve; pass += kUnroll * kThreads) {
             const int v0 = pass + threadIdx.x;
             uint4 raw[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int v = v0 + u * kThreads;
-                raw[u] = (v < nvec) ? __ldg(xt + v) : make_uint4(0u, 0u, 0u, 0u);
+                raw[u] = (v < ve) ? __ldg(xt + v) : make_uint4(0u, 0u, 0u, 0u);
             }
             uint2 q[kUnroll];
             float sc[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) q[u] = quant8(raw[u], &sc[u]);
-            if (pass == 0) place_token(ra, t, row, recv_src, s_row);
+            if (pass == vb) place_token(ra, t, row, recv_src, s_row, sl == 0);
             __syncthreads();
             for (int j = 0; j < ra.k; ++j) {
                 const int r = s_row[j];
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const int v = v0 + u * kThreads;
-                    if (v < nvec) {
+                    if (v < ve) {
                         dst[v] = q[u];
                         if ((lane & 15) == 0) sdst[v >> 4] = sc[u];
                     }
@@ -201,23 +212,26 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     }
 }
 
-// FP8 dispatch for rows of exactly NV * 128 vectors (H = 1024 * NV): no
-// bounds checks, and each token's NV * 8 scales go through shared memory so
-// every row's scales are one coalesced store.
+// FP8 dispatch for slices of exactly NV * 128 vectors (a row of
+// NV * 128 * nsplit vectors, H = 1024 * NV * nsplit): no bounds checks, and
+// the slice's NV * 8 scales go through shared memory so every row's scales
+// are one coalesced store.
 template <int NV>
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
-    RowArgs ra, const uint4* __restrict__ x, int32_t* __restrict__ row,
+    RowArgs ra, const uint4* __restrict__ x, int nsplit, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
     const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
 {
-    constexpr int nvec = NV * kThreads, nblk = nvec / 16;
+    constexpr int chunk = NV * kThreads, cblk = chunk / 16;
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    __shared__ float s_sc[nblk];
+    __shared__ float s_sc[cblk];
     if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
     const int tid = threadIdx.x;
-    for (int t = blockIdx.x; t < ra.T; t += gridDim.x) {
-        const uint4* xt = x + (size_t)t * nvec;
+    const int nvec = chunk * nsplit, nblk = cblk * nsplit;
+    for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
+        const int t = it / nsplit, sl = it - t * nsplit;
+        const uint4* xt = x + (size_t)t * nvec + sl * chunk;
         uint4 raw[NV];
 #pragma unroll
         for (int u = 0; u < NV; ++u) raw[u] = __ldg(xt + tid + u * kThreads);
@@ -228,15 +242,15 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
             q[u] = quant8(raw[u], &sc);
             if ((tid & 15) == 0) s_sc[(tid + u * kThreads) >> 4] = sc;
         }
-        place_token(ra, t, row, recv_src, s_row);
+        place_token(ra, t, row, recv_src, s_row, sl == 0);
         __syncthreads();
         for (int j = 0; j < ra.k; ++j) {
             const int r = s_row[j];
             if (r < 0) continue;
-            uint2* dst = recv_q + (size_t)r * nvec;
+            uint2* dst = recv_q + (size_t)r * nvec + sl * chunk;
 #pragma unroll
             for (int u = 0; u < NV; ++u) dst[tid + u * kThreads] = q[u];
-            if (tid < nblk) recv_scale[(size_t)r * nblk + tid] = s_sc[tid];
+            if (tid < cblk) recv_scale[(size_t)r * nblk + sl * cblk + tid] = s_sc[tid];
         }
         __syncthreads();
     }
@@ -244,20 +258,33 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
 
 }  // namespace
 
+int slices_for(int T, int units, int sm_count)
+{
+    if (T <= 0 || units <= 1) return 1;
+    const int want = (2 * sm_count + T - 1) / T;  // about two CTAs per SM
+    if (want <= 1) return 1;
+    for (int d = want; d <= units; ++d)
+        if (units % d == 0) return d;
+    return units;
+}
+
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
                             const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s)
 {
-    (void)sm_count;
     const int nvec = H / 8;
-    const int blocks = ra.T < 1 ? 1 : ra.T;
-    if (fp8 && nvec % kThreads == 0 && nvec / kThreads <= 8) {
+    const int T = ra.T < 1 ? 1 : ra.T;
+    if (fp8 && nvec % kThreads == 0 && nvec / kThreads <= 8 * 8) {
+        const int units = nvec / kThreads;  // 128-vector units of a row
+        const int nsplit = slices_for(T, units, sm_count);
+        if (units / nsplit <= 8) {
+            const int blocks = T * nsplit;
 #define MOEEP_FP8_FIT(N)                                                                         \
     case N:                                                                                      \
         return launch_pdl(dispatch_fp8_fit_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,      \
-                          (const uint4*)x, row, (uint2*)recv_x, recv_scale, recv_src, cnt,      \
-                          recv_cnt);
-        switch (nvec / kThreads) {
+                          (const uint4*)x, nsplit, row, (uint2*)recv_x, recv_scale, recv_src,   \
+                          cnt, recv_cnt);
+            switch (units / nsplit) {
             MOEEP_FP8_FIT(1)
             MOEEP_FP8_FIT(2)
             MOEEP_FP8_FIT(3)
@@ -266,15 +293,19 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
             MOEEP_FP8_FIT(6)
             MOEEP_FP8_FIT(7)
             MOEEP_FP8_FIT(8)
-        }
+            }
 #undef MOEEP_FP8_FIT
+        }
     }
+    // 128-element blocks (16 vectors) are the slicing unit of the other kernels
+    const int nsplit = (nvec % 16 == 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    const int blocks = T * nsplit;
     if (fp8)
         return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
-                          (const uint4*)x, nvec, row, (uint2*)recv_x, recv_scale, recv_src, cnt,
-                          recv_cnt);
+                          (const uint4*)x, nvec, nsplit, row, (uint2*)recv_x, recv_scale,
+                          recv_src, cnt, recv_cnt);
     return launch_pdl(dispatch_bf16_kernel, dim3(blocks), dim3(kThreads), s, ra, (const uint4*)x,
-                      nvec, row, (uint4*)recv_x, recv_src, cnt, recv_cnt);
+                      nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt);
 }
 
 }  // namespace moeep
