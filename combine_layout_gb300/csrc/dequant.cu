@@ -15,6 +15,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace moeep {
@@ -257,6 +259,27 @@ __global__ void __launch_bounds__(kThreads) dequant_tma_kernel(const int32_t* __
     }
 }
 
+// The TMA kernel's dynamic shared memory limit, raised once per device (the
+// attribute belongs to the device's copy of the kernel) and size.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_tma_smem[kMaxDevices];
+
+cudaError_t allow_tma_smem(int smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && g_tma_smem[dev].load() >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(dequant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        int cur = g_tma_smem[dev].load();
+        while (cur < smem && !g_tma_smem[dev].compare_exchange_weak(cur, smem)) {
+        }
+    }
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S, int mode, int H,
@@ -278,8 +301,7 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
         return launch_pdl(dequant_kernel, dim3(blocks), dim3(kThreads), s, cnt, off, E, S, mode,
                           H, (const uint4*)q, scale, (uint4*)y);
     }
-    cudaError_t e = cudaFuncSetAttribute(dequant_tma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = allow_tma_smem((int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl_smem(dequant_tma_kernel, dim3(sm_count * per_sm), dim3(kThreads), smem, s,
                            cnt, off, E, S, mode, H, q, scale, (uint4*)y, err);

@@ -224,7 +224,10 @@ MOE_EP_API int moe_ep_set_row_align(moe_ep_handle_t h, int align);
  * [recv_rows][H/128], y device bf16 [recv_rows][H] (16-byte aligned, may not
  * overlap recv_q).  No host synchronisation: the rows are enumerated on the
  * device from the counts.  Errors: MOE_EP_ERR_INVALID for H % 128 != 0,
- * misaligned pointers, too few rows, or no preceding moe_ep_route. */
+ * misaligned pointers, too few rows, or no preceding moe_ep_route.  Large
+ * batches stage rows in shared memory with bulk copies whose waits are
+ * bounded: a wait that gives up latches MOE_EP_DEVERR_TIMEOUT (the rows of
+ * that CTA are then incomplete), reported by the group's next call. */
 MOE_EP_API int moe_ep_dequant(moe_ep_handle_t h, const void* recv_q, const float* recv_scale,
                               void* y, int64_t recv_rows, moe_ep_stream_t stream);
 

@@ -118,3 +118,44 @@ def test_row_align_arguments():
     with pytest.raises(ep.MoeEpError):
         ep.moe_ep_set_row_align(q.handle, 64)     # LL layouts are slot-aligned already
     q.close()
+
+
+def test_fp8_dispatch_and_dequant_in_a_cuda_graph():
+    """Route, FP8 dispatch and the TMA-staged dequantisation (4096 tokens)
+    captured in a CUDA graph give, replayed on new scores, what eager calls give."""
+    w = synth.WORKLOADS["ht_prefill_fp8"]
+    inp = synth.make_inputs(w)
+    inp2 = synth.make_inputs(w, seed=w.seed + 1)
+    p = _pipe(w, 1, fp8=True)
+    scores = torch.from_numpy(inp["scores"]).to(DEV)
+    x = to_dev_bf16(inp["x"], DEV)
+    y = torch.zeros((p.rows, w.H), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+
+    def step():
+        p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode, stream=s)
+        p.dispatch(x, stream=s)
+        p.dequant(y, stream=s)
+
+    with torch.cuda.stream(s):
+        step()                          # eager: sets up what the launches need
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    scores.copy_(torch.from_numpy(inp2["scores"]))
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    got = bf16_bits(y).copy()
+    got_idx = p.topk_idx[: w.T].cpu().numpy()
+    y.zero_()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    assert np.array_equal(got_idx, p.topk_idx[: w.T].cpu().numpy())
+    assert np.array_equal(got, bf16_bits(y))
+    idx_o, _ = oracle.route(inp2["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+    assert np.array_equal(got_idx, idx_o)
+    assert p.device_errors() == 0
+    p.close()
