@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, partial_min_ctas(KMAX)) combine_part
             uint4 val[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (rr[j] >= 0) val[j] = __ldg(y + (size_t)rr[j] * nvec + v);
+                if (rr[j] >= 0) val[j] = __ldcs(y + (size_t)rr[j] * nvec + v);  // read once
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
                 const int q = s_q[j];  // block-uniform: the bookkeeping stays in shared memory
