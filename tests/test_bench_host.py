@@ -57,3 +57,23 @@ def test_algorithmic_bytes_per_unit():
     assert ab["combine"] == 4096 * (8 * (2 * 7168 + 8) + 2 * 7168)
     ab8 = bench.algorithmic_bytes(synth.WORKLOADS["ht_prefill_fp8"])
     assert ab8["dispatch"] == 4096 * (2 * 7168 + 32 + 8 * (7168 + 7168 // 32 + 4))
+
+
+def test_algorithmic_bytes_of_the_dedup_path():
+    """One copy per (token, rank) and its expansion; the two-stage combine
+    writes and reads one BF16 partial per dedup row.  With one dedup row per
+    pair (nothing to dedup) the dispatch side is the direct dispatch plus
+    every row written once more and read back (payload, token, mask), and
+    the combine side the direct combine plus the partials' round trip."""
+    import bench
+    from combine_layout_gb300 import synth
+    w = synth.WORKLOADS["ht_prefill"]
+    T, H, k = w.T, w.H, w.k
+    nd = 30574
+    ab = bench.algorithmic_bytes_dedup(w, nd)
+    assert ab["dispatch"] == T * (2 * H + 4 * k) + 2 * nd * (2 * H + 8) + T * k * (2 * H + 4)
+    assert ab["combine"] == T * k * (2 * H + 8) + 2 * nd * 2 * H + T * 2 * H
+    full = bench.algorithmic_bytes_dedup(w, T * k)
+    direct = bench.algorithmic_bytes(w)
+    assert full["dispatch"] == direct["dispatch"] + 2 * T * k * (2 * H + 8)
+    assert full["combine"] == direct["combine"] + 2 * T * k * 2 * H

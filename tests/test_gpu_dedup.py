@@ -179,3 +179,68 @@ def test_dedup_argument_errors():
     with pytest.raises(ep.MoeEpError):           # HT only
         q.dispatch_dedup(torch.zeros((32, 256), dtype=torch.bfloat16, device=DEV))
     q.close()
+
+
+def test_dedup_with_caller_routing_masked_and_invalid_ids():
+    """Caller-made routing with padding (-1), out-of-range and repeated ids:
+    the dedup rows skip them exactly as the oracle does, the expansion still
+    equals the direct dispatch, and the device error word latches the ids."""
+    import combine_layout_gb300.moe_ep as ep
+    from combine_layout_gb300.pipeline import EpPipeline
+    rng = np.random.default_rng(31)
+    T, E, R, H, k = 90, 32, 8, 256, 6
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    idx[::5, 2] = -1
+    idx[7, :] = -1
+    idx[11, 0] = E          # out of range
+    idx[13, 3] = idx[13, 1]  # repeated expert
+    x = synth.tokens_bf16(rng, T, H)
+    p = EpPipeline(synth.MODE_HT, E, R, T, H, k, device=DEV)
+    p.route_given(torch.from_numpy(idx).to(DEV))
+    torch.cuda.synchronize()
+    assert p.device_errors() & ep.MOE_EP_DEVERR_EXPERT_RANGE
+    p.clear_device_errors()
+    p.dispatch_dedup(to_dev_bf16(x, DEV))
+    p.recv_x.zero_()
+    p.expand()
+    torch.cuda.synchronize()
+    RL, st = oracle.rank_layout(idx, E, R)
+    assert st == oracle.ERR_INVALID
+    nd = int(RL["off"][-1])
+    assert np.array_equal(p.rank_off.cpu().numpy(), RL["off"])
+    assert np.array_equal(p.drecv_src[:nd].cpu().numpy(), RL["src"])
+    assert np.array_equal(p.drecv_mask[:nd].cpu().numpy().view(np.uint32), RL["mask"])
+    assert np.array_equal(bf16_bits(p.drecv_x[:nd]), x[RL["src"]])
+    D, _ = oracle.layout(idx, E, R, oracle.MODE_HT)
+    nrows = int(D["off"][-1])
+    want, _, want_src = oracle.dispatch(x, D["row"], nrows, fp8=False)
+    assert np.array_equal(bf16_bits(p.recv_x[:nrows]), want)
+    assert np.array_equal(p.recv_src[:nrows].cpu().numpy(), want_src)
+    w32 = rng.random((T, k)).astype(np.float32)
+    out = p.combine_dedup(p.recv_x, topk_w=torch.from_numpy(w32).to(DEV))
+    torch.cuda.synchronize()
+    want_out, part = oracle.combine_dedup(want, idx, D["row"], w32, E, R, RL["drow"], nd,
+                                          want_partial=True)
+    assert bf16_ulp_diff(bf16_bits(p.partial[:nd]), part).max() <= 1
+    assert np.all(bf16_bits(out)[7] == 0)                 # no pair: zero row
+    got = synth.bf16_bits_to_f32(bf16_bits(out)).astype(np.float64)
+    o = synth.bf16_bits_to_f32(want_out).astype(np.float64)
+    pu = _ulp(part)
+    for t in range(T):
+        qs = RL["drow"][t][RL["drow"][t] >= 0]
+        bound = pu[qs].sum(0) + np.maximum(_ulp(bf16_bits(out)[t]), _ulp(want_out[t]))
+        assert np.all(np.abs(got[t] - o[t]) <= bound * (1 + 1e-6)), t
+    assert p.device_errors() == 0
+    p.close()
+
+
+def test_dedup_empty_batch():
+    from combine_layout_gb300.pipeline import EpPipeline
+    p = EpPipeline(synth.MODE_HT, 16, 4, 64, 256, 4, device=DEV)
+    p.route(torch.zeros((0, 16), device=DEV), 0)
+    p.dispatch_dedup(torch.zeros((1, 256), dtype=torch.bfloat16, device=DEV))
+    p.expand()
+    p.combine_dedup(p.recv_x)
+    torch.cuda.synchronize()
+    assert p.rank_cnt.cpu().tolist() == [0] * 4 and p.rank_off.cpu().tolist() == [0] * 5
+    p.close()
