@@ -75,6 +75,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_EP_OK : MO
 inline int check_group(const moe_ep_group* g)
 {
     if (!g) return MOE_EP_ERR_INVALID;
+    if (g->err_host[kErrTimeout]) return MOE_EP_ERR_TIMEOUT;
     for (int i = 0; i < kErrSlots; ++i)
         if (g->err_host[i]) return MOE_EP_ERR_DEVICE;
     return MOE_EP_OK;
@@ -165,6 +166,7 @@ const char* moe_ep_status_string(int status)
         case MOE_EP_ERR_OVERFLOW: return "more tokens than max_tokens";
         case MOE_EP_ERR_CUDA: return "CUDA runtime error";
         case MOE_EP_ERR_DEVICE: return "device-error word set";
+        case MOE_EP_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
         default: return "unknown status";
     }
 }

@@ -18,9 +18,10 @@ LIB_PATH = os.path.join(_HERE, "libmoeep.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe_ep.h")
 
 MOE_EP_LL, MOE_EP_HT = 0, 1
-MOE_EP_OK, MOE_EP_ERR_INVALID, MOE_EP_ERR_OVERFLOW, MOE_EP_ERR_CUDA, MOE_EP_ERR_DEVICE = range(5)
+(MOE_EP_OK, MOE_EP_ERR_INVALID, MOE_EP_ERR_OVERFLOW, MOE_EP_ERR_CUDA, MOE_EP_ERR_DEVICE,
+ MOE_EP_ERR_TIMEOUT) = range(6)
 MOE_EP_W_SOFTMAX_TOPK, MOE_EP_W_SOFTMAX_RENORM, MOE_EP_W_SCORE_NORM = 0, 1, 2
-MOE_EP_DEVERR_EXPERT_RANGE, MOE_EP_DEVERR_DUPLICATE = 1, 2
+MOE_EP_DEVERR_EXPERT_RANGE, MOE_EP_DEVERR_DUPLICATE, MOE_EP_DEVERR_TIMEOUT = 1, 2, 4
 
 
 class MoeEpError(RuntimeError):

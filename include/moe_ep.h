@@ -27,8 +27,10 @@
  *    causes an out-of-bounds access: the pair is dropped and a bit is latched
  *    in the group's device-error word, which is visible to the host without a
  *    synchronisation once the kernel has finished; while it is set every call
- *    on the group returns MOE_EP_ERR_DEVICE until moe_ep_clear_device_errors.
- *    Kernels never trap and never wait on another kernel.
+ *    on the group returns MOE_EP_ERR_DEVICE (MOE_EP_ERR_TIMEOUT when a
+ *    bounded wait gave up) until moe_ep_clear_device_errors.
+ *    Kernels never trap and never wait on another kernel; the only waits are
+ *    on a CTA's own bulk copies, each bounded.
  *  - A handle's workspace is reused by each moe_ep_route call: use one handle
  *    per forward pass in flight (for instance one per layer).
  */
@@ -60,7 +62,9 @@ typedef enum {
     MOE_EP_ERR_INVALID = 1,  /* bad argument, shape or alignment */
     MOE_EP_ERR_OVERFLOW = 2, /* more tokens than the group's max_tokens (LL slots) */
     MOE_EP_ERR_CUDA = 3,     /* a CUDA runtime call or launch failed */
-    MOE_EP_ERR_DEVICE = 4    /* device-error word set (see moe_ep_get_device_errors) */
+    MOE_EP_ERR_DEVICE = 4,   /* device-error word set (see moe_ep_get_device_errors) */
+    MOE_EP_ERR_TIMEOUT = 5   /* device-error word holds MOE_EP_DEVERR_TIMEOUT: a
+                                bounded wait inside a kernel gave up */
 } moe_ep_status_t;
 
 /* Bits of the device-error word. */

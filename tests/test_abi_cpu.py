@@ -68,3 +68,4 @@ def test_host_argument_checks_without_gpu(lib):
     s = lib.moe_ep_status_string
     s.restype = ctypes.c_char_p
     assert s(0) == b"ok" and s(2).startswith(b"more tokens")
+    assert b"bounded wait" in s(5) and s(6) == b"unknown status"
