@@ -86,6 +86,16 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def workload_config(w: synth.Workload, world: int, rows: int) -> dict:
+    """The `config` of both arms' JSON lines (rows: receive-buffer rows)."""
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "ranks": w.R, "k": w.k,
+            "nodes": w.G, "max_nodes": w.kg,
+            "mode": "HT" if w.mode == synth.MODE_HT else "LL", "fp8": w.fp8,
+            "l2": "inputs larger than L2: each step writes and reads a "
+                  f"{rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer",
+            "parallelism": f"replicas x{world} (logical ranks inside each GPU)"}
+
+
 def kernel_source_sha(kernel: str) -> str:
     """Hash of a kernel's source file and the shared headers it includes."""
     csrc = os.path.join(ROOT, "combine_layout_gb300", "csrc")
@@ -391,12 +401,7 @@ def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
         "dtype": ("e4m3 dispatch payload, bf16 combine (fp32 accumulate)" if w.fp8
                   else "bf16 (fp32 combine accumulate)"),
         "data": "synthetic (seeded numpy: U[0,1)+U[0,0.5) per-expert bias scores, N(0,1) bf16 tokens)",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "ranks": w.R, "k": w.k,
-                   "nodes": w.G, "max_nodes": w.kg,
-                   "mode": "HT" if ht else "LL", "fp8": w.fp8,
-                   "l2": "inputs larger than L2: each step writes and reads a "
-                         f"{rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer",
-                   "parallelism": f"replicas x{world} (logical ranks inside each GPU)",
+        "config": {**workload_config(w, world, rows),
                    **({} if nd is None else {"path": "dedup", "dedup_rows": nd})},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "unit": "GB/s",
@@ -468,12 +473,13 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = T * args.steps / el
     sample = f"first {T} of {w.T} tokens per step (full H, E, k), {args.steps} steps"
-    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+    rows = w.E * w.slots if w.mode == synth.MODE_LL else w.T * w.k
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (fp32 FP8 decisions)",
             "data": "synthetic (seeded numpy)", "impl": "reference",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "ranks": w.R, "k": w.k,
-                       "mode": "HT" if w.mode == synth.MODE_HT else "LL", "fp8": w.fp8},
+            "config": workload_config(w, args.gpus, rows),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
