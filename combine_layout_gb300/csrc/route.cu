@@ -11,7 +11,9 @@
 // Scores are expected below 2^126 in magnitude, so a two-score sum cannot
 // overflow fp32.
 //
-// Work split: one warp per token, one CTA per 32-token tile.  Lane l holds up
+// Work split: one warp per token, one CTA per 32-token tile (batches up to
+// 1024 tokens: four CTAs of 8 tokens per tile, so more SMs share the
+// issue-bound selection).  Lane l holds up
 // to `epl` consecutive experts of group l / lpg, so a group's experts live in
 // lpg adjacent lanes and its top-m merges in log2(lpg) butterfly steps.  Each
 // of the k picks is two warp reductions (redux.sync): the largest score key,
