@@ -37,13 +37,13 @@ __device__ __forceinline__ uint32_t dequant_pair(uint16_t two_fp8, float s)
 __device__ __forceinline__ void count_prefix(const int32_t* __restrict__ cnt, int E, int* s_pre,
                                              int* s_part)
 {
-    const int tid = threadIdx.x;
-    const int per = (E + kThreads - 1) / kThreads;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (E + nt - 1) / nt;
     const int lo = min(tid * per, E), hi = min(lo + per, E);
     int sum = 0;
     for (int e = lo; e < hi; ++e) sum += __ldg(cnt + e);
     // block-wide exclusive scan of the per-thread sums: warp scans, then the
-    // warp totals (s_part holds the kThreads / 32 totals)
+    // warp totals (s_part holds the nt / 32 totals)
     const int lane = tid & 31, warp = tid >> 5;
     int incl = sum;
 #pragma unroll
@@ -55,7 +55,7 @@ __device__ __forceinline__ void count_prefix(const int32_t* __restrict__ cnt, in
     __syncthreads();
     int run = incl - sum;
     for (int w = 0; w < warp; ++w) run += s_part[w];
-    if (tid == kThreads - 1) s_pre[E] = run + sum;
+    if (tid == nt - 1) s_pre[E] = run + sum;
     for (int e = lo; e < hi; ++e) {
         s_pre[e] = run;
         run += __ldg(cnt + e);
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
 {
     griddep_wait();
     __shared__ int s_pre[kMaxExperts + 1];
-    __shared__ int s_part[kThreads];
+    __shared__ int s_part[32];
     const int tid = threadIdx.x;
     count_prefix(cnt, E, s_pre, s_part);
     const int total = s_pre[E];
@@ -138,6 +138,11 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const int32_t* __rest
 // still has in flight and returns.
 
 constexpr int kStages = 8;
+constexpr int kTmaMaxThreads = 512;
+// CTAs per SM (shared memory permitting).  Measured on the 4096-token,
+// 7168-wide FP8 layout: 3 CTAs x 8 stages 120 us; 2 x 8 139 us, 2 x 12
+// 137 us, 4 x 6 133 us, 6 x 4 130 us.
+constexpr int kTmaPerSm = 3;
 constexpr uint32_t kWaitPolls = 1u << 22;  // try_wait polls before a wait gives up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -180,7 +185,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return false;
 }
 
-__global__ void __launch_bounds__(kThreads) dequant_tma_kernel(const int32_t* __restrict__ cnt,
+__global__ void __launch_bounds__(kTmaMaxThreads) dequant_tma_kernel(const int32_t* __restrict__ cnt,
                                                                const int32_t* __restrict__ off,
                                                                int E, int S, int mode, int H,
                                                                const uint8_t* __restrict__ q,
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) dequant_tma_kernel(const int32_t* __
     __shared__ __align__(8) unsigned long long s_bar[kStages];
     __shared__ int s_row[kStages];
     __shared__ int s_pre[kMaxExperts + 1];
-    __shared__ int s_part[kThreads];
+    __shared__ int s_part[32];
     __shared__ int s_fail;
     const int tid = threadIdx.x;
     count_prefix(cnt, E, s_pre, s_part);
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) dequant_tma_kernel(const int32_t* __
             const uint4* qs = reinterpret_cast<const uint4*>(s_buf + (size_t)st * stage);
             const float* ss = reinterpret_cast<const float*>(s_buf + (size_t)st * stage + qbytes);
             uint4* yr = y + (size_t)s_row[st] * (H / 8);
-            for (int v = tid; v < nvq; v += kThreads) {
+            for (int v = tid; v < nvq; v += (int)blockDim.x) {
                 const uint4 w = qs[v];
                 const float sc = ss[v >> 3];
                 const uint32_t x[4] = {w.x, w.y, w.z, w.w};
@@ -288,7 +293,8 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
 {
     const size_t stage = (size_t)H + H / 32;
     const size_t smem = kStages * stage;
-    const int per_sm = smem <= 96 * 1024 ? 2 : 1;
+    int per_sm = (int)((200 * 1024) / smem);
+    per_sm = per_sm < 1 ? 1 : (per_sm > kTmaPerSm ? kTmaPerSm : per_sm);
     // staging pays once every CTA has rings of rows to stream; a small batch
     // (LL decode) is latency-bound and does better with a warp per row on
     // every SM, leaving shared memory to kernels of other streams
@@ -303,7 +309,10 @@ cudaError_t launch_dequant(const int32_t* cnt, const int32_t* off, int E, int S,
     }
     const cudaError_t e = allow_tma_smem((int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl_smem(dequant_tma_kernel, dim3(sm_count * per_sm), dim3(kThreads), smem, s,
+    // two vectors of a staged row per thread (the thread count matters little)
+    int thr = (H / 16 / 2 + 31) / 32 * 32;
+    thr = thr > kTmaMaxThreads ? kTmaMaxThreads : thr;
+    return launch_pdl_smem(dequant_tma_kernel, dim3(sm_count * per_sm), dim3(thr), smem, s,
                            cnt, off, E, S, mode, H, q, scale, (uint4*)y, err);
 }
 

@@ -59,7 +59,11 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
 }
 
 // Work items: token t's slice sl of nsplit equal column slices (nsplit = 1
-// except for small batches, where several CTAs share a token's rows).
+// except for small batches, where several CTAs share a token's rows).  U
+// vectors per thread per pass: the slice's own count where it fits in one
+// pass, so no registers are held for vectors a row does not have (fewer
+// registers, more CTAs per SM and more of the token rows in flight).
+template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
@@ -74,11 +78,11 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
         const int vb = sl * chunk, ve = vb + chunk;
         const uint4* xt = x + (size_t)t * nvec;
         // the pass loop is uniform across the CTA (it holds a barrier)
-        for (int pass = vb; pass < ve; pass += kUnroll * kThreads) {
+        for (int pass = vb; pass < ve; pass += U * kThreads) {
             const int v0 = pass + threadIdx.x;
-            uint4 buf[kUnroll];
+            uint4 buf[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int v = v0 + u * kThreads;
                 if (v < ve) buf[u] = __ldg(xt + v);
             }
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
                 if (r < 0) continue;
                 uint4* dst = recv_x + (size_t)r * nvec;
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
+                for (int u = 0; u < U; ++u) {
                     const int v = v0 + u * kThreads;
                     if (v < ve) dst[v] = buf[u];
                 }
@@ -304,8 +308,21 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
         return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
                           (const uint4*)x, nvec, nsplit, row, (uint2*)recv_x, recv_scale,
                           recv_src, cnt, recv_cnt);
-    return launch_pdl(dispatch_bf16_kernel, dim3(blocks), dim3(kThreads), s, ra, (const uint4*)x,
-                      nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt);
+    const int per = (nvec / nsplit + kThreads - 1) / kThreads;  // vectors per thread
+#define MOEEP_BF16(N)                                                                             \
+    return launch_pdl(dispatch_bf16_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,              \
+                      (const uint4*)x, nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt)
+    switch (per < kUnroll ? per : kUnroll) {
+    case 1: MOEEP_BF16(1);
+    case 2: MOEEP_BF16(2);
+    case 3: MOEEP_BF16(3);
+    case 4: MOEEP_BF16(4);
+    case 5: MOEEP_BF16(5);
+    case 6: MOEEP_BF16(6);
+    case 7: MOEEP_BF16(7);
+    default: MOEEP_BF16(kUnroll);
+    }
+#undef MOEEP_BF16
 }
 
 }  // namespace moeep
