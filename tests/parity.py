@@ -4,10 +4,17 @@ Tolerances, derived from the arithmetic:
   - routing indices, counts, offsets, row map, receive rows, FP8 bytes and
     scales, source ids: bit-exact (integer / byte work, and the FP8 code is
     decided by one fp32 division on both sides).
-  - gate weights: the kernel computes in fp32, the oracle in binary64.  A sum
-    of k <= 8 positive fp32 terms plus one division is within (k+1) units of
-    2^-24 relative; softmax adds expf's error (<= 2 ulp) and one more
-    division.  Bound used: 32 * 2^-24 relative (~1.9e-6).
+  - gate weights: the kernel computes in fp32, the oracle in binary64; u =
+    2^-24.  Score-normalised: a sum of k positive terms ((k-1) roundings)
+    and one division, within k u relative.  Softmax over the top k: each
+    exp(v - max) carries the fp32 subtraction's error (at most d u in the
+    exponent, d the distance of v from the maximum) and expf's (<= 2 ulp,
+    4 u), in the numerator and, averaged, in the sum; then k - 1 additions
+    and one division: 2 (d + 4) u + k u.  Renormalised full softmax: the
+    normaliser cancels in the ratio, leaving one more division per selected
+    term, k u more.  Bound used (w_rtol): max(32, 2k + 2 (d + 4) + 2) u, d
+    the largest distance between a token's best score and its selected
+    scores -- 32 u (~1.9e-6) for the workloads (k <= 8, d <= 4).
   - combine: the kernel accumulates k fp32 fused multiply-adds and rounds once
     to bf16; the oracle sums exactly-representable products in binary64 and
     rounds once.  The fp32 error (< k * 2^-24 relative) can move the result
@@ -21,6 +28,16 @@ import torch
 from combine_layout_gb300 import synth
 
 W_RTOL = 32 * 2.0 ** -24
+
+
+def w_rtol(k: int, scores: np.ndarray | None = None, idx: np.ndarray | None = None) -> float:
+    """Relative tolerance of the gate weights (module docstring); d is taken
+    from the fp32 scores and the selected expert ids when given."""
+    d = 0.0
+    if scores is not None and idx is not None and scores.size and idx.size:
+        sel = np.take_along_axis(scores.astype(np.float64), np.maximum(idx, 0).astype(np.int64), 1)
+        d = float((scores.max(1).astype(np.float64) - sel.min(1)).max())
+    return max(32.0, 2 * k + 2 * (d + 4) + 2) * 2.0 ** -24
 
 
 def to_dev_bf16(bits: np.ndarray, dev) -> torch.Tensor:

@@ -15,8 +15,8 @@ import torch
 
 import oracle
 from combine_layout_gb300 import synth
-from parity import (W_RTOL, bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device,
-                    identity_rows, to_dev_bf16)
+from parity import (bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device,
+                    identity_rows, to_dev_bf16, w_rtol)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _check_route_layout(w, p, inp):
     wg = p.topk_w[: w.T].cpu().numpy()
     idx_o, w_o = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
     assert np.array_equal(idx, idx_o), "topk_idx differs"
-    np.testing.assert_allclose(wg, w_o, rtol=W_RTOL, atol=0)
+    np.testing.assert_allclose(wg, w_o, rtol=w_rtol(w.k, inp["scores"], idx_o), atol=0)
     L = {k: v.cpu().numpy() for k, v in p.layout().items()}
     L_o, st = oracle.layout(idx_o, w.E, w.R, w.mode, w.slots)
     assert st == oracle.OK
