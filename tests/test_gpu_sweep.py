@@ -6,7 +6,9 @@ score distribution and gate-weight rule, and runs the whole path (route,
 layout, receive-count query, dispatch, combine) against the oracle element
 by element, as the workload parity tests do.  Routing constraints follow the
 router's: groups of E/G experts, k <= kg * E/G, m = ceil(k / kg) <= 4 scores
-per group when the node limit is on, at most 16 experts per lane.
+per group when the node limit is on, at most 16 experts per lane.  The
+per-rank dedup path (HT, at most 32 local experts per rank) is swept the
+same way through its own parity check.
 """
 from __future__ import annotations
 
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 
 from combine_layout_gb300 import synth
+from test_gpu_dedup import _run as _run_dedup
 from test_gpu_parity import _run
 
 pytestmark = pytest.mark.gpu
@@ -26,7 +29,7 @@ def _lanes_per_group(G: int) -> int:
     return lpg
 
 
-def _cases(n: int = 24, seed: int = 2024):
+def _cases(n: int = 24, seed: int = 2024, dedup: bool = False):
     rng = np.random.default_rng(seed)
     out = []
     while len(out) < n:
@@ -42,28 +45,40 @@ def _cases(n: int = 24, seed: int = 2024):
         limit = G > 1 and kg < G
         if limit and -(-k // kg) > min(4, gs):
             continue
-        R = int(rng.choice([d for d in range(1, E + 1) if E % d == 0]))
+        R = int(rng.choice([d for d in range(1, E + 1)
+                            if E % d == 0 and (not dedup or E // d <= 32)]))
         fp8 = bool(rng.random() < 0.5)
         H = int(rng.choice([128, 256, 384, 640, 1024, 2048])) if fp8 else \
             int(rng.choice([8, 24, 136, 256, 712, 1024, 4104]))
-        mode = synth.MODE_HT if rng.random() < 0.5 else synth.MODE_LL
+        mode = synth.MODE_HT if dedup or rng.random() < 0.5 else synth.MODE_LL
         T = int(rng.integers(1, 700))
         scores = str(rng.choice(["uniform_bias", "uniform_raw", "zipf_bias", "normal_logits"]))
         # score-normalised weights need positive scores
         wm = int(rng.choice([synth.W_SOFTMAX_TOPK, synth.W_SOFTMAX_RENORM] +
                             ([synth.W_SCORE_NORM] if scores != "normal_logits" else [])))
         out.append(synth.Workload(
-            f"sweep{len(out)}", T=T, H=H, E=E, R=R, k=k, mode=mode, fp8=fp8, scores=scores,
-            weight_mode=wm, G=G, kg=kg, slots=T if mode == synth.MODE_LL else 0,
+            f"{'dedup' if dedup else 'sweep'}{len(out)}", T=T, H=H, E=E, R=R, k=k, mode=mode,
+            fp8=fp8, scores=scores, weight_mode=wm, G=G, kg=kg,
+            slots=T if mode == synth.MODE_LL else 0,
             seed=int(rng.integers(1 << 30))))
     return out
 
 
+def _ids(cases):
+    return [f"{c.name}-E{c.E}R{c.R}G{c.G}kg{c.kg}k{c.k}H{c.H}T{c.T}"
+            f"{'LL' if c.mode == synth.MODE_LL else 'HT'}{'fp8' if c.fp8 else ''}w{c.weight_mode}"
+            for c in cases]
+
+
 CASES = _cases()
+DEDUP_CASES = _cases(12, seed=77, dedup=True)
 
 
-@pytest.mark.parametrize("w", CASES, ids=[f"{c.name}-E{c.E}R{c.R}G{c.G}kg{c.kg}k{c.k}H{c.H}T{c.T}"
-                                          f"{'LL' if c.mode == synth.MODE_LL else 'HT'}"
-                                          f"{'fp8' if c.fp8 else ''}w{c.weight_mode}" for c in CASES])
+@pytest.mark.parametrize("w", CASES, ids=_ids(CASES))
 def test_parity_sweep(w):
     _run(w)
+
+
+@pytest.mark.parametrize("w", DEDUP_CASES, ids=_ids(DEDUP_CASES))
+def test_dedup_parity_sweep(w):
+    _run_dedup(w)
