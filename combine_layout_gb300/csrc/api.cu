@@ -59,6 +59,8 @@ struct moe_ep_handle {
     // state of the last route
     int routed;
     int rows_ready;       // row[] written for the last route
+    int words_only;       // the last route's layout is deferred: tile words only (small LL batch)
+    int layout_pending;   // ... and its counts and offsets are not computed yet
     int T, k;
     int64_t host_total;   // total rows known on the host (-1: not queried)
     int align;            // HT expert blocks padded to a multiple of align rows
@@ -143,7 +145,20 @@ RowArgs row_args(const moe_ep_handle* h)
     a.ncols = a.E;
     a.mask = nullptr;
     a.off_out = nullptr;
+    a.from_words = h->words_only;
     return a;
+}
+
+// The counts and offsets of a deferred layout, before a consumer that reads
+// them without a dispatch having produced them.
+int ensure_counts(moe_ep_handle* h, cudaStream_t s)
+{
+    if (!h->layout_pending) return MOE_EP_OK;
+    LayoutArgs la = layout_args(h, h->T);
+    la.deferred = 1;
+    int st = cuda_status(launch_finish_words(la, s));
+    if (st == MOE_EP_OK) h->layout_pending = 0;
+    return st;
 }
 
 int ensure_rows(moe_ep_handle* h, cudaStream_t s)
@@ -308,6 +323,8 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->has_sent = 0;
     h->routed = 0;
     h->rows_ready = 0;
+    h->words_only = 0;
+    h->layout_pending = 0;
     h->dedup_ready = 0;
     h->host_total = -1;
     h->align = 1;
@@ -342,6 +359,9 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (T > 0 && !topk_idx) return MOE_EP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
     LayoutArgs la = layout_args(h, T);
+    // LL batches of at most kDeferMaxTiles tiles: no serial tail after the
+    // router; the dispatch's first CTA finishes the counts and offsets
+    la.deferred = (g->mode == MOE_EP_LL && T > 0 && la.ntiles <= kDeferMaxTiles) ? 1 : 0;
     if (g->mode == MOE_EP_HT && T > 0) {
         // the layout publishes the counts for the receive-count query
         la.host_out = h->host_counts_dev;
@@ -388,6 +408,8 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (la.host_out) h->seq = la.seq;
     h->routed = 1;
     h->rows_ready = 0;
+    h->words_only = la.deferred;
+    h->layout_pending = la.deferred;
     h->dedup_ready = 0;
     h->T = T;
     h->k = k;
@@ -467,10 +489,14 @@ int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, flo
     }
     if (recv_src && ((uintptr_t)recv_src & 3u)) return MOE_EP_ERR_INVALID;
     if (recv_cnt && ((uintptr_t)recv_cnt & 3u)) return MOE_EP_ERR_INVALID;
+    LayoutArgs fin = layout_args(h, h->T);
     st = cuda_status(launch_dispatch(row_args(h), x, g->H, fp8, h->row, recv_x, recv_scale,
                                      recv_src, h->cnt, recv_cnt, g->sm_count,
-                                     (cudaStream_t)stream));
-    if (st == MOE_EP_OK) h->rows_ready = 1;
+                                     (cudaStream_t)stream, h->layout_pending ? &fin : nullptr));
+    if (st == MOE_EP_OK) {
+        h->rows_ready = 1;
+        h->layout_pending = 0;
+    }
     return st;
 }
 
@@ -552,6 +578,8 @@ int moe_ep_dequant(moe_ep_handle_t h, const void* recv_q, const float* recv_scal
     if (!recv_q || !recv_scale || !y || !aligned16(recv_q) || !aligned16(y) ||
         ((uintptr_t)recv_scale & 3u))
         return MOE_EP_ERR_INVALID;
+    st = ensure_counts(h, (cudaStream_t)stream);
+    if (st != MOE_EP_OK) return st;
     return cuda_status(launch_dequant(h->cnt, h->off, g->E, g->S, g->mode, g->H,
                                       (const uint8_t*)recv_q, recv_scale, y,
                                       (int64_t)h->T * h->k, g->sm_count, g->err_dev,
@@ -772,6 +800,8 @@ int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off, int32_t* r
         int st = ensure_rows(h, s);
         if (st != MOE_EP_OK) return st;
     }
+    int st = ensure_counts(h, s);
+    if (st != MOE_EP_OK) return st;
     cudaError_t e = cudaSuccess;
     if (cnt && e == cudaSuccess)
         e = cudaMemcpyAsync(cnt, h->cnt, sizeof(int32_t) * g->E, cudaMemcpyDefault, s);

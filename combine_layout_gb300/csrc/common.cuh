@@ -11,6 +11,11 @@ namespace moeep {
 // Layout tiles hold 32 tokens so that one expert's presence in a tile is one
 // 32-bit word (bit i = token tile*32 + i chose that expert).
 constexpr int kTileTokens = 32;
+// Tiles per group of the layout's byte counts.
+constexpr int kGroupTiles = 16;
+// The most tiles of a deferred LL layout (LayoutArgs.deferred): its
+// consumers sum the earlier tiles' words directly, two loads at a time.
+constexpr int kDeferMaxTiles = 8;
 constexpr int kMaxTopk = 32;
 constexpr int kMaxGroups = 32;
 constexpr int kMaxGroupTopk = 4;
@@ -99,6 +104,12 @@ struct LayoutArgs {
     // bytes of several CTAs); the last CTA derives tile_cnt from the words
     // and writes it.  Only with ntiles <= 32 (at most two groups).
     int cnt_from_words = 0;
+    // 1: the producers write only tile_word and skip the last-CTA tail; the
+    // layout's consumers rank pairs from the words (RowArgs.from_words) and
+    // the first of them finishes cnt / off / rcnt / roff
+    // (finish_layout_from_words).  LL layouts of at most kDeferMaxTiles
+    // tiles only.
+    int deferred = 0;
     // Optional publication of the counts to the host (mapped pinned memory,
     // device alias): off[E+1], rcnt[R], cnt[E], then the sequence number
     // `seq`, written last, after a system-scope fence.  nullptr: none.
@@ -120,6 +131,7 @@ struct RowArgs {
     int ncols;                 // E / G
     uint32_t* mask;            // G > 1: per row, bit l = local expert l of the token (may be null)
     int32_t* off_out;          // dispatch: copy of off[0 .. ncols] (may be null)
+    int from_words = 0;        // 1: rank pairs from the tile words alone (deferred LL layout)
 };
 
 // What the receiver side of the per-rank dedup path needs: the expert layout
@@ -156,16 +168,23 @@ cudaError_t launch_layout_bits(const int32_t* topk_idx, int T, int k, int32_t* i
 // layout copy that comes without a dispatch).
 cudaError_t launch_rowmap(const RowArgs& ra, int32_t* row, int sm_count, cudaStream_t s);
 
+// Counts and offsets of a deferred layout (la.deferred) from its tile words:
+// one CTA (the dispatch does the same in its first CTA).
+cudaError_t launch_finish_words(const LayoutArgs& la, cudaStream_t s);
+
 // Column slices per token for small batches: the smallest divisor of
 // `units` (equal slices of a row) that puts about two CTAs on every SM;
 // 1 when the tokens alone do.
 int slices_for(int T, int units, int sm_count);
 
 // Dispatch pack: x bf16 [T][H] -> receive rows (bf16 copy or FP8 + scales).
-// Also writes the row map and recv_src, and copies cnt into recv_cnt.
+// Also writes the row map and recv_src, and copies cnt into recv_cnt -- or,
+// with fin != nullptr (a deferred layout), its first CTA finishes the
+// layout's counts and offsets from the tile words and writes recv_cnt.
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
-                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s);
+                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s,
+                            const LayoutArgs* fin = nullptr);
 
 // Node-level layout (node counts, offsets, rows with GPU masks) and the
 // routing statistics (stats may be null; otherwise 4 sums, accumulated).

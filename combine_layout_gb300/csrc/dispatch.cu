@@ -28,10 +28,16 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kThreads = 128;
 constexpr int kUnroll = 8;  // 16-byte vectors per thread per pass (H <= 8192 in one pass)
 
-// CTA 0: the caller's copies of the column counts and offsets.
+// CTA 0: the caller's copies of the column counts and offsets; with a
+// deferred layout, first the layout's counts and offsets from the tile words
+// (the router left that to the first consumer).
 __device__ __forceinline__ void copy_counts(const RowArgs& ra, const int32_t* cnt,
-                                            int32_t* recv_cnt)
+                                            int32_t* recv_cnt, const LayoutArgs& fin)
 {
+    if (fin.deferred) {
+        finish_layout_from_words<kThreads>(fin, recv_cnt);
+        return;
+    }
     for (int c = threadIdx.x; c <= ra.ncols; c += blockDim.x) {
         if (recv_cnt && c < ra.ncols) recv_cnt[c] = cnt[c];
         if (ra.off_out) ra.off_out[c] = ra.off[c];
@@ -67,11 +73,11 @@ template <int U>
 __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
-    int32_t* __restrict__ recv_cnt)
+    int32_t* __restrict__ recv_cnt, LayoutArgs fin)
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt, fin);
     const int chunk = nvec / nsplit;
     for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
         const int t = it / nsplit, sl = it - t * nsplit;
@@ -169,11 +175,11 @@ __device__ __forceinline__ uint2 quant8(const uint4& raw, float* scale_out)
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
-    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
+    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt, LayoutArgs fin)
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt, fin);
     const int lane = threadIdx.x & 31;
     const int nblk = nvec / 16;
     const int chunk = nvec / nsplit;  // a multiple of 16 vectors: whole 128-blocks
@@ -224,13 +230,13 @@ template <int NV>
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nsplit, int32_t* __restrict__ row,
     uint2* __restrict__ recv_q, float* __restrict__ recv_scale, int32_t* __restrict__ recv_src,
-    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt)
+    const int32_t* __restrict__ cnt, int32_t* __restrict__ recv_cnt, LayoutArgs fin)
 {
     constexpr int chunk = NV * kThreads, cblk = chunk / 16;
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
     __shared__ float s_sc[cblk];
-    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt);
+    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt, fin);
     const int tid = threadIdx.x;
     const int nvec = chunk * nsplit, nblk = cblk * nsplit;
     for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
@@ -274,8 +280,12 @@ int slices_for(int T, int units, int sm_count)
 
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
-                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s)
+                            const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s,
+                            const LayoutArgs* fin_in)
 {
+    LayoutArgs fin{};
+    if (fin_in) fin = *fin_in;
+    fin.deferred = fin_in ? 1 : 0;
     const int nvec = H / 8;
     const int T = ra.T < 1 ? 1 : ra.T;
     if (fp8 && nvec % kThreads == 0 && nvec / kThreads <= 8 * 8) {
@@ -287,7 +297,7 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
     case N:                                                                                      \
         return launch_pdl(dispatch_fp8_fit_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,      \
                           (const uint4*)x, nsplit, row, (uint2*)recv_x, recv_scale, recv_src,   \
-                          cnt, recv_cnt);
+                          cnt, recv_cnt, fin);
             switch (units / nsplit) {
             MOEEP_FP8_FIT(1)
             MOEEP_FP8_FIT(2)
@@ -307,11 +317,11 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
     if (fp8)
         return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
                           (const uint4*)x, nvec, nsplit, row, (uint2*)recv_x, recv_scale,
-                          recv_src, cnt, recv_cnt);
+                          recv_src, cnt, recv_cnt, fin);
     const int per = (nvec / nsplit + kThreads - 1) / kThreads;  // vectors per thread
 #define MOEEP_BF16(N)                                                                             \
     return launch_pdl(dispatch_bf16_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,              \
-                      (const uint4*)x, nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt)
+                      (const uint4*)x, nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt, fin)
     switch (per < kUnroll ? per : kUnroll) {
     case 1: MOEEP_BF16(1);
     case 2: MOEEP_BF16(2);

@@ -24,8 +24,6 @@
 
 namespace moeep {
 
-constexpr int kGroupTiles = 16;
-
 // Shared memory the layout tail needs (ints): per-part sums, warp sums,
 // per-expert counts and offsets.
 constexpr int kTailSmemInts = 1024 + 32 + 2 * kMaxExperts;
@@ -279,6 +277,74 @@ __device__ __forceinline__ void finish_layout_if_last(const LayoutArgs& a, int* 
     }
 }
 
+// Deferred LL layout (LayoutArgs.deferred: a few tiles, no padding),
+// finished by one CTA of NT threads from the tile words alone:
+// cnt[e] = sum over tiles of popc(word), off = exclusive prefix, rank counts
+// and offsets from the expert offsets, recv_cnt (may be null) = cnt.  All
+// NT threads of the CTA must call it (it holds barriers).  The words are
+// spread over the threads, 8 loads in flight each, and summed per expert in
+// shared memory: few registers, since the dispatch kernels inline this into
+// their first CTA.
+template <int NT>
+__device__ __forceinline__ void finish_layout_from_words(const LayoutArgs& a, int32_t* recv_cnt)
+{
+    static_assert(NT % 32 == 0, "block size");
+    constexpr int kU = 8;
+    __shared__ int s_warp[NT / 32];
+    __shared__ int s_cnt[kMaxExperts + 1];  // counts, then (in place) offsets
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E;
+    for (int e = tid; e < E; e += NT) s_cnt[e] = 0;
+    __syncthreads();
+    const int nw = a.ntiles * E;
+    for (int q0 = tid; q0 < nw; q0 += NT * kU) {
+        uint32_t w[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * NT;
+            w[u] = q < nw ? __ldcg(a.tile_word + q) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * NT;
+            if (q < nw && w[u]) atomicAdd(&s_cnt[q - (q / E) * E], __popc(w[u]));
+        }
+    }
+    __syncthreads();
+    const int per = (E + NT - 1) / NT;
+    const int lo = min(tid * per, E), hi = min(lo + per, E);
+    int sum = 0;
+    for (int e = lo; e < hi; ++e) sum += s_cnt[e];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += s_warp[w];
+    for (int e = lo; e < hi; ++e) {
+        const int c = s_cnt[e];
+        a.cnt[e] = c;
+        a.off[e] = run;
+        if (recv_cnt) recv_cnt[e] = c;
+        s_cnt[e] = run;  // this thread's own experts: offsets in place of counts
+        run += c;
+    }
+    if (lo < E && hi == E) {  // the thread holding the last expert: the total
+        a.off[E] = run;
+        s_cnt[E] = run;
+    }
+    __syncthreads();
+    const int L = E / a.R;
+    for (int r = tid; r <= a.R; r += NT) {
+        a.roff[r] = s_cnt[r * L];
+        if (r < a.R) a.rcnt[r] = s_cnt[(r + 1) * L] - s_cnt[r * L];
+    }
+}
+
 // Receive row of pair (t, lane) for lanes < k of a warp (-1 for lanes >= k and
 // for pairs without a row).  All 32 lanes must call it (warp-collective).
 // Invalid pairs -- id outside [0, E), or an expert repeated at an earlier j of
@@ -308,9 +374,14 @@ __device__ __forceinline__ int token_pair_row(const RowArgs& a, int t, int lane,
     *mask = m;
     if (!valid) return -1;
     const int tile = t / kTileTokens;
-    const int rank =
-        pairs_before_tile(a.tile_cnt, a.grp_base, a.ncols, col, tile) +
-        __popc(__ldg(a.tile_word + (size_t)tile * a.ncols + col) & ((1u << (t & 31)) - 1u));
+    int rank = __popc(__ldg(a.tile_word + (size_t)tile * a.ncols + col) & ((1u << (t & 31)) - 1u));
+    if (a.from_words) {  // a few tiles: the earlier tiles' words, two loads in flight
+#pragma unroll 2
+        for (int tl = 0; tl < tile; ++tl)
+            rank += __popc(__ldg(a.tile_word + (size_t)tl * a.ncols + col));
+    } else {
+        rank += pairs_before_tile(a.tile_cnt, a.grp_base, a.ncols, col, tile);
+    }
     return (a.mode == MOE_EP_HT) ? __ldg(a.off + col) + rank : col * a.S + rank;
 }
 

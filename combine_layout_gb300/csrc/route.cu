@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(TPC * 32, TPC == kTileTokens ? 1 : 2) route_ke
         }
     }
     griddep_launch_dependents();
-    finish_layout_if_last(la, s_scratch);
+    if (!la.deferred) finish_layout_if_last(la, s_scratch);
 }
 
 __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restrict__ topk_idx,
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restr
         la.tile_cnt[tile_cnt_index(tile, e, E)] = (uint8_t)__popc(wd);
     }
     griddep_launch_dependents();
-    finish_layout_if_last(la, s_scratch);
+    if (!la.deferred) finish_layout_if_last(la, s_scratch);
 }
 
 template <int EPL, bool VEC>
