@@ -234,3 +234,61 @@ def test_router_adversarial_scores(E, G, kg, k, m):
     bad = np.nonzero((got != idx_o).any(1))[0]
     assert bad.size == 0, (bad[:5], got[bad[:2]], idx_o[bad[:2]])
     p.close()
+
+
+@pytest.mark.parametrize("T", [1, 31, 33, 128, 255, 256, 257])
+def test_ll_small_batch_layout_without_dispatch(T):
+    """Small LL batches leave the counts and offsets to the first consumer:
+    the layout copy, a combine and a dequantisation that come before any
+    dispatch, and a second dispatch of the same route, all see the oracle's
+    layout (256 tokens and fewer; 257 takes the router's own tail)."""
+    E, R, S, H, k, G, kg = 64, 8, 300, 256, 6, 8, 3
+    rng = np.random.default_rng(T)
+    s = synth.uniform_bias_scores(rng, T, E)
+    x = synth.tokens_bf16(rng, T, H)
+    idx_o, w_o = oracle.route(s, k, G, kg)
+    L_o, st = oracle.layout(idx_o, E, R, synth.MODE_LL, S)
+    assert st == oracle.OK
+    sc = torch.from_numpy(s).to(DEV)
+
+    # layout copy straight after the route
+    p = _pipe(synth.MODE_LL, E, R, S, H, k)
+    p.route(sc, T, G, kg)
+    L = {key: v.cpu().numpy() for key, v in p.layout().items()}
+    for key in ("cnt", "off", "rcnt", "roff", "row"):
+        assert np.array_equal(L[key], L_o[key]), key
+    # combine before any dispatch: rows from the words; y holds each pair's token
+    y = np.zeros((E * S, H), np.uint16)
+    flat = L_o["row"].ravel()
+    y[flat] = x[np.arange(T * k) // k]
+    w32 = np.ascontiguousarray(w_o, dtype=np.float32)
+    p2 = _pipe(synth.MODE_LL, E, R, S, H, k)
+    p2.route(sc, T, G, kg)
+    out = p2.combine(to_dev_bf16(y, DEV), topk_w=torch.from_numpy(w32).to(DEV))
+    torch.cuda.synchronize()
+    want = oracle.combine(y, L_o["row"], w32)
+    assert bf16_ulp_diff(bf16_bits(out[:T]), want).max() <= 1
+    # two dispatches of one route: the counts are right both times
+    for _ in range(2):
+        p2.recv_cnt.fill_(-1)
+        p2.dispatch(to_dev_bf16(x, DEV))
+        torch.cuda.synchronize()
+        assert np.array_equal(p2.recv_cnt.cpu().numpy(), L_o["cnt"])
+        got = bf16_bits(p2.recv_x[torch.from_numpy(flat.astype(np.int64)).to(DEV)])
+        assert np.array_equal(got, x[np.arange(T * k) // k])
+    p.close()
+    p2.close()
+
+    # dequantisation before any dispatch writes exactly the defined slots
+    p3 = _pipe(synth.MODE_LL, E, R, S, H, k, fp8=True)
+    p3.route(sc, T, G, kg)
+    p3.recv_x.zero_()
+    p3.recv_scale.fill_(1.0)
+    yq = torch.full((E * S, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    p3.dequant(yq)
+    torch.cuda.synchronize()
+    defined = np.zeros(E * S, bool)
+    defined[flat] = True
+    got = yq.float().cpu().numpy()
+    assert np.all(got[defined] == 0.0) and np.all(np.isnan(got[~defined]))
+    p3.close()
