@@ -13,7 +13,9 @@
 //
 // Work split: one warp per token, one CTA per 32-token tile (batches up to
 // 1024 tokens: four CTAs of 8 tokens per tile, so more SMs share the
-// issue-bound selection).  Lane l holds up
+// issue-bound selection).  The grid's last CTA finishes the layout, except
+// for a deferred LL layout (at most 256 tokens), which the dispatch's first
+// CTA finishes from the tile words.  Lane l holds up
 // to `epl` consecutive experts of group l / lpg, so a group's experts live in
 // lpg adjacent lanes and its top-m merges in log2(lpg) butterfly steps.  Each
 // of the k picks is two warp reductions (redux.sync): the largest score key,
