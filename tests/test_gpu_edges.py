@@ -292,3 +292,56 @@ def test_ll_small_batch_layout_without_dispatch(T):
     got = yq.float().cpu().numpy()
     assert np.all(got[defined] == 0.0) and np.all(np.isnan(got[~defined]))
     p3.close()
+
+
+@pytest.mark.parametrize("T", [70, 300])
+def test_ll_caller_routing_masked_repeated_and_invalid(T):
+    """Caller routing in LL mode (70 tokens: the deferred layout; 300: the
+    router's tail): masked pairs get no slot and no combine term, invalid and
+    repeated ids latch the device-error word and get no slot, and nothing is
+    written outside the defined slots."""
+    ep = _ep()
+    E, R, H, k = 16, 4, 128, 3
+    S = T
+    rng = np.random.default_rng(T)
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    idx[::5, 1] = -1
+    idx[7, :] = -1
+    idx[3, 0] = E           # out of range
+    idx[9, 2] = -4          # out of range
+    idx[12, 2] = idx[12, 0]  # repeated expert
+    x = synth.tokens_bf16(rng, T, H)
+    p = _pipe(synth.MODE_LL, E, R, S, H, k)
+    guard = torch.full((p.rows + 64, H), 7, dtype=torch.bfloat16, device=DEV)
+    p.recv_x = guard[: p.rows]
+    p.route_given(torch.from_numpy(idx).to(DEV))
+    torch.cuda.synchronize()
+    bits = p.device_errors()
+    assert bits & ep.MOE_EP_DEVERR_EXPERT_RANGE and bits & ep.MOE_EP_DEVERR_DUPLICATE
+    p.clear_device_errors()
+    L_o, st = oracle.layout(idx, E, R, oracle.MODE_LL, S)
+    assert st == oracle.ERR_INVALID
+    p.dispatch(to_dev_bf16(x, DEV))
+    w_h = rng.random((T, k)).astype(np.float32)
+    out = p.combine(p.recv_x, torch.from_numpy(w_h).to(DEV))
+    torch.cuda.synchronize()
+    L = {key: v.cpu().numpy() for key, v in p.layout().items()}
+    for key in ("cnt", "off", "rcnt", "roff", "row"):
+        assert np.array_equal(L[key], L_o[key]), key
+    assert np.array_equal(p.recv_cnt.cpu().numpy(), L_o["cnt"])
+    # defined slots hold their tokens; every other row keeps the guard
+    defined = np.zeros(p.rows + 64, bool)
+    rows = L_o["row"][L_o["row"] >= 0]
+    defined[rows] = True
+    g = bf16_bits(guard)
+    assert np.all(g[~defined] == bf16_bits(torch.full((1,), 7, dtype=torch.bfloat16))[0])
+    tok = np.nonzero(L_o["row"] >= 0)[0]
+    assert np.array_equal(g[L_o["row"][L_o["row"] >= 0]], x[tok])
+    # combine: no term for pairs without a slot
+    y = np.zeros((p.rows, H), np.uint16)
+    y[rows] = x[tok]
+    want = oracle.combine(y, L_o["row"], w_h)
+    assert bf16_ulp_diff(bf16_bits(out[:T]), want).max() <= 1
+    assert np.all(bf16_bits(out)[7] == 0)
+    assert p.device_errors() == 0
+    p.close()
