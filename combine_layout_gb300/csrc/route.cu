@@ -288,6 +288,103 @@ __global__ void __launch_bounds__(TPC * 32, TPC == kTileTokens ? 1 : 2) route_ke
     if (!la.deferred) finish_layout_if_last(la, s_scratch);
 }
 
+// Small expert counts without a node limit (E <= W, W = 8 or 16 lanes per
+// token): 32 / W tokens per warp, one expert per lane of the token's W-lane
+// segment, so no lane of the warp idles while E is far below 32.  A CTA of W
+// warps routes one 32-token tile.  The selection and the weights are those of
+// route_token: each pick is the largest key, then the lowest expert index
+// holding it (here a butterfly over the segment); the weights' sums run in the
+// same order (the j-ordered sums lane by lane; the full-softmax normaliser by
+// the same butterfly levels, the lanes past E adding zeros), so for a single
+// routing group both kernels give the same bits.
+template <int W>
+__global__ void __launch_bounds__(W * 32) route_small_kernel(
+    const float* __restrict__ scores, int T, RouteParams p, int32_t* __restrict__ topk_idx,
+    int32_t* __restrict__ idx_copy, float* __restrict__ topk_w, LayoutArgs la)
+{
+    constexpr int kTpw = 32 / W;  // tokens per warp
+    griddep_wait();
+    __shared__ uint32_t s_word[kMaxExperts];
+    __shared__ int s_scratch[kTailSmemInts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sl = lane & (W - 1);  // the lane's expert (and output slot j)
+    for (int e = tid; e < p.E; e += blockDim.x) s_word[e] = 0u;
+    __syncthreads();
+
+    const int tile = blockIdx.x;
+    const int slot = warp * kTpw + lane / W;  // the token's bit in its tile word
+    const int t = tile * kTileTokens + slot;
+    const bool tok = t < T;
+    const bool in = tok && sl < p.E;
+    const uint32_t key0 = in ? score_key(__ldg(scores + (size_t)t * p.E + sl)) : 0u;
+    uint32_t key = key0;
+    int my_i = -1;
+    uint32_t my_k = 0u, first_k = 0u;
+    float den = 0.f;
+    for (int j = 0; j < p.k; ++j) {
+        uint32_t bk = key;
+        int bi = key ? sl : W;  // no candidate: past every index
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) {
+            const uint32_t ok = __shfl_xor_sync(kFull, bk, o, W);
+            const int oi = __shfl_xor_sync(kFull, bi, o, W);
+            if (ok > bk || (ok == bk && oi < bi)) {
+                bk = ok;
+                bi = oi;
+            }
+        }
+        const bool found = bk != 0u;
+        if (found && sl == bi) key = 0u;  // the winner leaves the candidates
+        if (sl == j) {
+            my_i = found ? bi : -1;
+            my_k = bk;
+        }
+        if (j == 0) first_k = bk;
+        den += key_score(bk);
+    }
+
+    const bool act = sl < p.k;
+    const float my_v = key_score(my_k);
+    const int base = lane & ~(W - 1);  // the segment's first lane
+    float w;
+    if (p.wmode == MOE_EP_W_SCORE_NORM) {
+        w = __fdiv_rn(my_v, den);
+    } else if (p.wmode == MOE_EP_W_SOFTMAX_TOPK) {
+        const float mx = key_score(first_k);
+        const float ex = act ? expf(my_v - mx) : 0.f;
+        float d = 0.f;
+        for (int j = 0; j < p.k; ++j) d += __shfl_sync(kFull, ex, base + j);
+        w = __fdiv_rn(ex, d);
+    } else {
+        uint32_t mloc = in ? key0 : 0u;
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) mloc = max(mloc, __shfl_xor_sync(kFull, mloc, o, W));
+        const float mx = key_score(mloc);
+        float z = in ? expf(key_score(key0) - mx) : 0.f;
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o, W);
+        const float pj = act ? __fdiv_rn(expf(my_v - mx), z) : 0.f;
+        float sel = 0.f;
+        for (int j = 0; j < p.k; ++j) sel += __shfl_sync(kFull, pj, base + j);
+        w = __fdiv_rn(pj, sel);
+    }
+    if (tok && act) {
+        const size_t q = (size_t)t * p.k + sl;
+        topk_idx[q] = my_i;
+        idx_copy[q] = my_i;
+        if (topk_w) topk_w[q] = w;
+        if (my_i >= 0) atomicOr(&s_word[my_i], 1u << slot);
+    }
+    __syncthreads();
+    for (int e = tid; e < p.E; e += blockDim.x) {
+        const uint32_t wd = s_word[e];
+        la.tile_word[(size_t)tile * p.E + e] = wd;
+        la.tile_cnt[tile_cnt_index(tile, e, p.E)] = (uint8_t)__popc(wd);
+    }
+    griddep_launch_dependents();
+    if (!la.deferred) finish_layout_if_last(la, s_scratch);
+}
+
 __global__ void __launch_bounds__(256) layout_bits_kernel(const int32_t* __restrict__ topk_idx,
                                                           int T, int k,
                                                           int32_t* __restrict__ idx_copy,
@@ -371,6 +468,14 @@ cudaError_t launch_route(const float* scores, int T, const RouteParams& p, int32
                          int32_t* idx_copy, float* topk_w, const LayoutArgs& la, cudaStream_t s)
 {
     if (T <= 0) return cudaSuccess;
+    if (!p.limit && p.E <= 16) {  // small expert counts: several tokens per warp
+        const int ntiles = (T + kTileTokens - 1) / kTileTokens;
+        if (p.E <= 8)
+            return launch_pdl(route_small_kernel<8>, dim3(ntiles), dim3(8 * 32), s, scores, T, p,
+                              topk_idx, idx_copy, topk_w, tail_planned(la, 8 * 32));
+        return launch_pdl(route_small_kernel<16>, dim3(ntiles), dim3(16 * 32), s, scores, T, p,
+                          topk_idx, idx_copy, topk_w, tail_planned(la, 16 * 32));
+    }
     if (p.epl <= 1) return launch_route_epl<1>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     if (p.epl <= 2) return launch_route_epl<2>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
     if (p.epl <= 4) return launch_route_epl<4>(scores, T, p, topk_idx, idx_copy, topk_w, la, s);
