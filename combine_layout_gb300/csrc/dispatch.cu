@@ -31,11 +31,12 @@ constexpr int kUnroll = 8;  // 16-byte vectors per thread per pass (H <= 8192 in
 // CTA 0: the caller's copies of the column counts and offsets; with a
 // deferred layout, first the layout's counts and offsets from the tile words
 // (the router left that to the first consumer).
+template <int NT = kThreads>
 __device__ __forceinline__ void copy_counts(const RowArgs& ra, const int32_t* cnt,
                                             int32_t* recv_cnt, const LayoutArgs& fin)
 {
     if (fin.deferred) {
-        finish_layout_from_words<kThreads>(fin, recv_cnt);
+        finish_layout_from_words<NT>(fin, recv_cnt);
         return;
     }
     for (int c = threadIdx.x; c <= ra.ncols; c += blockDim.x) {
@@ -68,28 +69,31 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
 // except for small batches, where several CTAs share a token's rows).  U
 // vectors per thread per pass: the slice's own count where it fits in one
 // pass, so no registers are held for vectors a row does not have (fewer
-// registers, more CTAs per SM and more of the token rows in flight).
-template <int U>
-__global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
+// registers, more CTAs per SM and more of the token rows in flight).  NT
+// threads: 128, or 64 for rows of at most 512 vectors (H <= 4096), so that a
+// CTA still holds U = 8 vectors per thread and an SM holds as many bytes of
+// token rows in flight as with wider rows.
+template <int U, int NT>
+__global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
     int32_t* __restrict__ recv_cnt, LayoutArgs fin)
 {
     griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0) copy_counts(ra, cnt, recv_cnt, fin);
+    if (blockIdx.x == 0) copy_counts<NT>(ra, cnt, recv_cnt, fin);
     const int chunk = nvec / nsplit;
     for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
         const int t = it / nsplit, sl = it - t * nsplit;
         const int vb = sl * chunk, ve = vb + chunk;
         const uint4* xt = x + (size_t)t * nvec;
         // the pass loop is uniform across the CTA (it holds a barrier)
-        for (int pass = vb; pass < ve; pass += U * kThreads) {
+        for (int pass = vb; pass < ve; pass += U * NT) {
             const int v0 = pass + threadIdx.x;
             uint4 buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * kThreads;
+                const int v = v0 + u * NT;
                 if (v < ve) buf[u] = __ldg(xt + v);
             }
             if (pass == vb) place_token(ra, t, row, recv_src, s_row, sl == 0);
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(
                 uint4* dst = recv_x + (size_t)r * nvec;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int v = v0 + u * kThreads;
+                    const int v = v0 + u * NT;
                     if (v < ve) dst[v] = buf[u];
                 }
             }
@@ -318,20 +322,28 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
         return launch_pdl(dispatch_fp8_kernel, dim3(blocks), dim3(kThreads), s, ra,
                           (const uint4*)x, nvec, nsplit, row, (uint2*)recv_x, recv_scale,
                           recv_src, cnt, recv_cnt, fin);
-    const int per = (nvec / nsplit + kThreads - 1) / kThreads;  // vectors per thread
-#define MOEEP_BF16(N)                                                                             \
-    return launch_pdl(dispatch_bf16_kernel<N>, dim3(blocks), dim3(kThreads), s, ra,              \
-                      (const uint4*)x, nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt, fin)
-    switch (per < kUnroll ? per : kUnroll) {
-    case 1: MOEEP_BF16(1);
-    case 2: MOEEP_BF16(2);
-    case 3: MOEEP_BF16(3);
-    case 4: MOEEP_BF16(4);
-    case 5: MOEEP_BF16(5);
-    case 6: MOEEP_BF16(6);
-    case 7: MOEEP_BF16(7);
-    default: MOEEP_BF16(kUnroll);
+    const int chunk = nvec / nsplit;
+    const bool narrow = chunk <= kUnroll * 64;  // 64 threads of up to 8 vectors
+    const int nt = narrow ? 64 : kThreads;
+    int per = (chunk + nt - 1) / nt;  // vectors per thread
+    per = per < kUnroll ? per : kUnroll;
+#define MOEEP_BF16(N, T_)                                                                         \
+    return launch_pdl(dispatch_bf16_kernel<N, T_>, dim3(blocks), dim3(T_), s, ra, (const uint4*)x, \
+                      nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt, fin)
+#define MOEEP_BF16_ALL(T_)           \
+    switch (per) {                   \
+    case 1: MOEEP_BF16(1, T_);       \
+    case 2: MOEEP_BF16(2, T_);       \
+    case 3: MOEEP_BF16(3, T_);       \
+    case 4: MOEEP_BF16(4, T_);       \
+    case 5: MOEEP_BF16(5, T_);       \
+    case 6: MOEEP_BF16(6, T_);       \
+    case 7: MOEEP_BF16(7, T_);       \
+    default: MOEEP_BF16(kUnroll, T_); \
     }
+    if (narrow) MOEEP_BF16_ALL(64);
+    MOEEP_BF16_ALL(kThreads);
+#undef MOEEP_BF16_ALL
 #undef MOEEP_BF16
 }
 
