@@ -213,7 +213,11 @@ def run_gpu(args) -> dict | None:
     x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     scores = scores_h.to(dev)
     x = x_h.to(dev)
-    p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=dev)
+    # x is resident (or, end to end, uploaded) before each step's route and
+    # nothing writes it between the route and the dispatch: the MoE-layer
+    # order, so the dispatch may read its tokens while the router finishes
+    p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=dev,
+                   x_before_route=True)
     if w.fp8:
         g = torch.Generator(device=dev)
         g.manual_seed(1234 + rank)
@@ -433,6 +437,7 @@ def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
         },
         "e2e": e2e,
         "gpu_launches": (KERNELS_PER_STEP if nd is None else KERNELS_PER_STEP_DEDUP) * args.steps,
+        "x_before_route": True,
         "clocks": clk,
         "round_trip_max_abs_err": rt,
     }

@@ -64,6 +64,7 @@ struct moe_ep_handle {
     int T, k;
     int64_t host_total;   // total rows known on the host (-1: not queried)
     int align;            // HT expert blocks padded to a multiple of align rows
+    int x_early;          // x is complete before the route (moe_ep_set_x_before_route)
     cudaEvent_t sent;     // recorded after a send-only dispatch / combine
     int has_sent;
 };
@@ -328,6 +329,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->dedup_ready = 0;
     h->host_total = -1;
     h->align = 1;
+    h->x_early = 0;
     g->handles += 1;
     *out = h;
     return MOE_EP_OK;
@@ -492,7 +494,8 @@ int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, flo
     LayoutArgs fin = layout_args(h, h->T);
     st = cuda_status(launch_dispatch(row_args(h), x, g->H, fp8, h->row, recv_x, recv_scale,
                                      recv_src, h->cnt, recv_cnt, g->sm_count,
-                                     (cudaStream_t)stream, h->layout_pending ? &fin : nullptr));
+                                     (cudaStream_t)stream, h->layout_pending ? &fin : nullptr,
+                                     h->x_early));
     if (st == MOE_EP_OK) {
         h->rows_ready = 1;
         h->layout_pending = 0;
@@ -561,6 +564,13 @@ int moe_ep_set_row_align(moe_ep_handle_t h, int align)
     if (!h || align < 1 || align > 1024 || (align & (align - 1)) != 0) return MOE_EP_ERR_INVALID;
     if (h->g->mode != MOE_EP_HT && align != 1) return MOE_EP_ERR_INVALID;
     h->align = align;
+    return MOE_EP_OK;
+}
+
+int moe_ep_set_x_before_route(moe_ep_handle_t h, int on)
+{
+    if (!h || (on != 0 && on != 1)) return MOE_EP_ERR_INVALID;
+    h->x_early = on;
     return MOE_EP_OK;
 }
 
@@ -710,7 +720,7 @@ int moe_ep_dispatch_dedup(moe_ep_handle_t h, const void* x, int fp8, void* drecv
             ra.mask = drecv_mask;
             ra.off_out = rank_off;
             e = launch_dispatch(ra, x, g->H, fp8, h->drow, drecv_x, drecv_scale, drecv_src,
-                                h->rk_cnt, rank_cnt, g->sm_count, s);
+                                h->rk_cnt, rank_cnt, g->sm_count, s, nullptr, h->x_early);
         }
     }
     if (T == 0) {

@@ -181,10 +181,13 @@ int slices_for(int T, int units, int sm_count);
 // Also writes the row map and recv_src, and copies cnt into recv_cnt -- or,
 // with fin != nullptr (a deferred layout), its first CTA finishes the
 // layout's counts and offsets from the tile words and writes recv_cnt.
+// early: x was complete before the layout's producer started, so each bf16
+// CTA reads its first token before waiting for that producer (the FP8
+// kernels read after the wait: measured no faster with the early read).
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
                             const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s,
-                            const LayoutArgs* fin = nullptr);
+                            const LayoutArgs* fin = nullptr, int early = 0);
 
 // Node-level layout (node counts, offsets, rows with GPU masks) and the
 // routing statistics (stats may be null; otherwise 4 sums, accumulated).

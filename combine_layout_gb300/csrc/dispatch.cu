@@ -65,51 +65,60 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
     }
 }
 
-// Work items: token t's slice sl of nsplit equal column slices (nsplit = 1
-// except for small batches, where several CTAs share a token's rows).  U
-// vectors per thread per pass: the slice's own count where it fits in one
-// pass, so no registers are held for vectors a row does not have (fewer
-// registers, more CTAs per SM and more of the token rows in flight).  NT
-// threads: 128, or 64 for rows of at most 512 vectors (H <= 4096), so that a
-// CTA still holds U = 8 vectors per thread and an SM holds as many bytes of
-// token rows in flight as with wider rows.
+// One CTA per work item: token t's slice sl of nsplit equal column slices
+// (nsplit = 1 except for small batches, where several CTAs share a token's
+// rows; the grid is exactly T * nsplit CTAs).  U vectors per thread per
+// pass: the slice's own count where it fits in one pass, so no registers are
+// held for vectors a row does not have (fewer registers, more CTAs per SM and
+// more of the token rows in flight).  NT threads: 128, or 64 for rows of at
+// most 512 vectors (H <= 4096), so that a CTA still holds U = 8 vectors per
+// thread and an SM holds as many bytes of token rows in flight as with wider
+// rows.  early: x was complete before the layout's producer started, so the
+// first pass is read before waiting for that producer (while the router
+// finishes the layout).
 template <int U, int NT>
 __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, int nsplit, int32_t* __restrict__ row,
     uint4* __restrict__ recv_x, int32_t* __restrict__ recv_src, const int32_t* __restrict__ cnt,
-    int32_t* __restrict__ recv_cnt, LayoutArgs fin)
+    int32_t* __restrict__ recv_cnt, LayoutArgs fin, int early)
 {
-    griddep_wait();
     __shared__ int s_row[kMaxTopk];
-    if (blockIdx.x == 0) copy_counts<NT>(ra, cnt, recv_cnt, fin);
     const int chunk = nvec / nsplit;
-    for (int it = blockIdx.x; it < ra.T * nsplit; it += gridDim.x) {
-        const int t = it / nsplit, sl = it - t * nsplit;
-        const int vb = sl * chunk, ve = vb + chunk;
-        const uint4* xt = x + (size_t)t * nvec;
-        // the pass loop is uniform across the CTA (it holds a barrier)
-        for (int pass = vb; pass < ve; pass += U * NT) {
-            const int v0 = pass + threadIdx.x;
-            uint4 buf[U];
+    const bool item = (int)blockIdx.x < ra.T * nsplit;
+    const int t = blockIdx.x / nsplit, sl = blockIdx.x - t * nsplit;
+    const int vb = sl * chunk, ve = vb + chunk;
+    const uint4* xt = x + (size_t)t * nvec;
+    uint4 buf[U];
+    auto load = [&](int pass) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = pass + threadIdx.x + u * NT;
+            if (v < ve) buf[u] = __ldg(xt + v);
+        }
+    };
+    auto store = [&](int pass) {
+        for (int j = 0; j < ra.k; ++j) {
+            const int r = s_row[j];
+            if (r < 0) continue;
+            uint4* dst = recv_x + (size_t)r * nvec;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * NT;
-                if (v < ve) buf[u] = __ldg(xt + v);
-            }
-            if (pass == vb) place_token(ra, t, row, recv_src, s_row, sl == 0);
-            __syncthreads();
-            for (int j = 0; j < ra.k; ++j) {
-                const int r = s_row[j];
-                if (r < 0) continue;
-                uint4* dst = recv_x + (size_t)r * nvec;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int v = v0 + u * NT;
-                    if (v < ve) dst[v] = buf[u];
-                }
+                const int v = pass + threadIdx.x + u * NT;
+                if (v < ve) dst[v] = buf[u];
             }
         }
-        __syncthreads();
+    };
+    if (early && item) load(vb);
+    griddep_wait();
+    if (blockIdx.x == 0) copy_counts<NT>(ra, cnt, recv_cnt, fin);
+    if (!item) return;
+    if (!early) load(vb);
+    place_token(ra, t, row, recv_src, s_row, sl == 0);
+    __syncthreads();
+    store(vb);
+    for (int pass = vb + U * NT; pass < ve; pass += U * NT) {  // rows wider than one pass
+        load(pass);
+        store(pass);
     }
 }
 
@@ -285,7 +294,7 @@ int slices_for(int T, int units, int sm_count)
 cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, int32_t* row,
                             void* recv_x, float* recv_scale, int32_t* recv_src,
                             const int32_t* cnt, int32_t* recv_cnt, int sm_count, cudaStream_t s,
-                            const LayoutArgs* fin_in)
+                            const LayoutArgs* fin_in, int early)
 {
     LayoutArgs fin{};
     if (fin_in) fin = *fin_in;
@@ -329,7 +338,7 @@ cudaError_t launch_dispatch(const RowArgs& ra, const void* x, int H, int fp8, in
     per = per < kUnroll ? per : kUnroll;
 #define MOEEP_BF16(N, T_)                                                                         \
     return launch_pdl(dispatch_bf16_kernel<N, T_>, dim3(blocks), dim3(T_), s, ra, (const uint4*)x, \
-                      nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt, fin)
+                      nvec, nsplit, row, (uint4*)recv_x, recv_src, cnt, recv_cnt, fin, early)
 #define MOEEP_BF16_ALL(T_)           \
     switch (per) {                   \
     case 1: MOEEP_BF16(1, T_);       \

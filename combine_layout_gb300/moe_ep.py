@@ -57,6 +57,7 @@ def _load() -> ctypes.CDLL:
         "moe_ep_clear_device_errors": [P],
         "moe_ep_node_layout": [P, I, I, P, P, P, P, I64, P, P],
         "moe_ep_set_row_align": [P, I],
+        "moe_ep_set_x_before_route": [P, I],
         "moe_ep_dispatch_send": [P, P, I, P, P, P, P, I64, P],
         "moe_ep_combine_send": [P, P, P, P, I64, P],
         "moe_ep_complete": [P, P],
@@ -207,6 +208,11 @@ def moe_ep_complete(handle: int, stream=None) -> None:
 
 def moe_ep_set_row_align(handle: int, align: int) -> None:
     _check("moe_ep_set_row_align", _lib.moe_ep_set_row_align(ctypes.c_void_p(handle), align))
+
+
+def moe_ep_set_x_before_route(handle: int, on: bool) -> None:
+    _check("moe_ep_set_x_before_route",
+           _lib.moe_ep_set_x_before_route(ctypes.c_void_p(handle), 1 if on else 0))
 
 
 def moe_ep_dequant(handle: int, recv_q, recv_scale, y, recv_rows: int | None = None,

@@ -14,7 +14,8 @@ from . import moe_ep as ep
 
 class EpPipeline:
     def __init__(self, mode: int, experts: int, ranks: int, max_tokens: int, hidden: int,
-                 topk: int, fp8: bool = False, device: str | int = "cuda", align: int = 1):
+                 topk: int, fp8: bool = False, device: str | int = "cuda", align: int = 1,
+                 x_before_route: bool = False):
         self.mode, self.E, self.R, self.S, self.H, self.k = mode, experts, ranks, max_tokens, hidden, topk
         self.fp8 = fp8
         self.device = torch.device(device)
@@ -22,6 +23,8 @@ class EpPipeline:
         self.handle = ep.moe_ep_create_handle(self.group, topk)
         if align != 1:
             ep.moe_ep_set_row_align(self.handle, align)
+        if x_before_route:
+            ep.moe_ep_set_x_before_route(self.handle, True)
         self.align = align
         self.rows = (experts * max_tokens if mode == ep.MOE_EP_LL
                      else max_tokens * topk + experts * (align - 1))

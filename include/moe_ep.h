@@ -219,6 +219,19 @@ MOE_EP_API int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream);
  * only align = 1 is accepted in LL mode.  Host only, no synchronisation. */
 MOE_EP_API int moe_ep_set_row_align(moe_ep_handle_t h, int align);
 
+/* Declare (on = 1) that for every dispatch on this handle the tokens x were
+ * complete before the moe_ep_route that made the handle's layout was
+ * enqueued, on the same stream -- as in an MoE layer, where x is the input of
+ * the gate that produces the scores.  A bf16 dispatch (moe_ep_dispatch,
+ * moe_ep_dispatch_send, moe_ep_dispatch_dedup) then reads each CTA's first
+ * token while the router is still finishing the layout, instead of after it
+ * (FP8 dispatch is unaffected).  Results are the same either way; with on = 1
+ * and an x written after the route was enqueued (for instance by a kernel
+ * launched between the route and the dispatch) the dispatch may read stale
+ * tokens.  Default 0.
+ * Host only, no synchronisation. */
+MOE_EP_API int moe_ep_set_x_before_route(moe_ep_handle_t h, int on);
+
 /* Receive-side dequantisation of an FP8 dispatch: for every row the last
  * route's layout defines (HT: expert blocks without their padding; LL: slots
  * below each expert's count), y[row] = bf16_rn(float(q[row]) * scale), the

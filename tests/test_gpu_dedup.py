@@ -33,10 +33,11 @@ def _ulp(bits):
     return 2.0 ** (np.floor(np.log2(np.maximum(f, 2.0 ** -126))) - 7)
 
 
-def _run(w, sample=None):
+def _run(w, sample=None, x_early=False):
     from combine_layout_gb300.pipeline import EpPipeline
     inp = synth.make_inputs(w)
-    p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV)
+    p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV,
+                   x_before_route=x_early)
     x_d = to_dev_bf16(inp["x"], DEV)
     p.route(torch.from_numpy(inp["scores"]).to(DEV), w.T, w.G, w.kg, 0, w.weight_mode)
     p.dispatch_dedup(x_d)
@@ -140,6 +141,11 @@ def test_dedup_elementwise(name, T):
 def test_dedup_full_size(name):
     nd, nrows = _run(synth.WORKLOADS[name], sample=1024)
     assert nd < nrows
+
+
+@pytest.mark.parametrize("name", ["ht_prefill", "ht_prefill_fp8"])
+def test_dedup_with_x_before_route(name):
+    _run(synth.WORKLOADS[name].with_tokens(300), x_early=True)
 
 
 def test_dedup_small_ranks_wide_masks():

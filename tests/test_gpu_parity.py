@@ -23,9 +23,10 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def _pipeline(w):
+def _pipeline(w, x_early=False):
     from combine_layout_gb300.pipeline import EpPipeline
-    return EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV)
+    return EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV,
+                      x_before_route=x_early)
 
 
 def _check_route_layout(w, p, inp):
@@ -42,9 +43,9 @@ def _check_route_layout(w, p, inp):
     return idx_o, w_o, L_o
 
 
-def _run(w, sample=None, seed=None):
+def _run(w, sample=None, seed=None, x_early=False):
     inp = synth.make_inputs(w, seed)
-    p = _pipeline(w)
+    p = _pipeline(w, x_early)
     scores = torch.from_numpy(inp["scores"]).to(DEV)
     x = to_dev_bf16(inp["x"], DEV)
     p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode)
@@ -124,6 +125,24 @@ def test_parity_elementwise(name, T):
                                   "mixtral", "skewed"])
 def test_parity_full_size(name):
     _run(synth.WORKLOADS[name], sample=1024)
+
+
+@pytest.mark.parametrize("name,T,H", [("tiny_ll", 77, None), ("ll_decode", 128, None),
+                                      ("ht_prefill", 300, None), ("ht_prefill_fp8", 300, None),
+                                      ("ht_prefill_fp8", 300, 640), ("mixtral", 1000, None),
+                                      ("ht_prefill", 4096, None), ("ht_prefill_fp8", 4096, None)])
+def test_parity_with_x_before_route(name, T, H):
+    """moe_ep_set_x_before_route: each bf16 dispatch CTA reads its token
+    before waiting for the router; the results are the same (the FP8 cases,
+    general kernel at H = 640 and exact-fit at 7168, read after the wait)."""
+    base = synth.WORKLOADS[name]
+    w = base.with_tokens(T, slots=base.slots or None)
+    if H is not None:
+        d = dict(w.__dict__)
+        d.pop("extra")
+        d["H"] = H
+        w = synth.Workload(**d)
+    _run(w, sample=1024 if T > 1000 else None, x_early=True)
 
 
 def test_fp8_conversion_sweep_all_bf16_values():
