@@ -168,6 +168,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
             gk = sum_key(gsum);
         }
         int rank = 0;
+#pragma unroll 8
         for (int n = 0; n < p.G; ++n) {
             const unsigned long long o = __shfl_sync(kFull, gk, n << p.lpg_log2);
             rank += (o > gk || (o == gk && n < grp)) ? 1 : 0;
@@ -187,6 +188,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
     int my_i = -1;
     uint32_t my_k = 0u, first_k = 0u;
     float den = 0.f;
+#pragma unroll 8
     for (int j = 0; j < p.k; ++j) {
         const uint32_t hk = key[0];
         const uint32_t mk = __reduce_max_sync(kFull, hk);
