@@ -96,13 +96,23 @@ def workload_config(w: synth.Workload, world: int, rows: int) -> dict:
             "parallelism": f"replicas x{world} (logical ranks inside each GPU)"}
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without its comments and with whitespace runs folded:
+    a comment edit does not change the kernel (string literals in these
+    sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of a kernel's source file and the shared headers it includes."""
+    """Hash of the code (not the comments) of a kernel's source file and of
+    the shared headers it includes."""
     csrc = os.path.join(ROOT, "combine_layout_gb300", "csrc")
     h = hashlib.sha256()
     for name in (f"{kernel}.cu", "common.cuh", "layout_dev.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -33,9 +33,11 @@ constexpr int kErrTimeout = 2;  // a bounded wait inside a kernel gave up
 // the stream is still finishing (launch latency and that kernel's tail
 // overlap), and each kernel executes griddep_wait() before its first global
 // memory access, which returns once the kernels before it have completed and
-// their writes are visible.  Kernels that produce a layout signal their
-// dependents as soon as every CTA has written its tile (the grid's last CTA
-// then finishes the layout while the next kernel's CTAs are being placed).
+// their writes are visible (the one exception: the bf16 dispatch's token
+// loads when the caller declared x complete before the route).  Kernels that
+// produce a layout signal their dependents as soon as every CTA has written
+// its tile (the grid's last CTA then finishes the layout while the next
+// kernel's CTAs are being placed).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                             cudaStream_t s, Args... args)
