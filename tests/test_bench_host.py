@@ -77,3 +77,14 @@ def test_algorithmic_bytes_of_the_dedup_path():
     direct = bench.algorithmic_bytes(w)
     assert full["dispatch"] == direct["dispatch"] + 2 * T * k * (2 * H + 8)
     assert full["combine"] == direct["combine"] + 2 * T * k * 2 * H
+
+
+def test_profile_hash_ignores_comments_only():
+    """The hash tying an ncu summary to its kernel source sees code changes,
+    not comment or whitespace edits."""
+    import bench
+    a = "int f(int x) {\n    return x + 1;  // add one\n}\n/* block\n comment */"
+    b = "int f(int x)\n{\n  return x + 1;\n}\n// other words"
+    c = "int f(int x) { return x + 2; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
