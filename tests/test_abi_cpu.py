@@ -65,6 +65,10 @@ def test_host_argument_checks_without_gpu(lib):
         g = getattr(lib, name)
         g.argtypes = [ctypes.c_void_p]
         assert g(None) == INVALID
+    for name in ("moe_ep_set_row_align", "moe_ep_set_x_before_route"):
+        g = getattr(lib, name)
+        g.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        assert g(None, 1) == INVALID
     s = lib.moe_ep_status_string
     s.restype = ctypes.c_char_p
     assert s(0) == b"ok" and s(2).startswith(b"more tokens")
