@@ -13,7 +13,8 @@
 //
 // Work split: one warp per token, one CTA per 32-token tile (batches up to
 // 1024 tokens: four CTAs of 8 tokens per tile, so more SMs share the
-// issue-bound selection).  The grid's last CTA finishes the layout, except
+// issue-bound selection; 16 experts or fewer without a node limit: 2 or 4
+// tokens per warp, route_small_kernel).  The grid's last CTA finishes the layout, except
 // for a deferred LL layout (at most 256 tokens), which the dispatch's first
 // CTA finishes from the tile words.  Lane l holds up
 // to `epl` consecutive experts of group l / lpg, so a group's experts live in
