@@ -3,8 +3,9 @@ seeded inputs, for the five workloads.
 
 Reduced token counts (several 32-token tiles plus a ragged tail) are compared
 element by element; the full-size workloads, in the launch configuration the
-benchmark times, compare routing and layout in full and dispatch / combine on
-sampled rows and tokens the oracle computes one by one.  Tolerances: see
+benchmark times (including its moe_ep_set_x_before_route declaration, in
+test_parity_with_x_before_route), compare routing and layout in full and
+dispatch / combine on sampled rows and tokens the oracle computes one by one.  Tolerances: see
 tests/parity.py.
 """
 from __future__ import annotations
