@@ -182,6 +182,7 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
         for (int e = 0; e < E; ++e) {
             allowed[e] = 1;
             sv[e] = isnan(s_in[e]) ? -INFINITY : s_in[e];   /* NaN ranks as -infinity */
+            if (sv[e] == 0.0f) sv[e] = 0.0f;                 /* -0 is the score 0 */
         }
         const float* s = sv;
 
@@ -223,12 +224,16 @@ int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k
         qsort(cand, (size_t)nc, sizeof(scored), by_value_desc);
         for (int j = 0; j < k; ++j) topk_idx[t * k + j] = cand[j].i;
 
-        /* Step 3: gate weights (binary64). */
+        /* Step 3: gate weights.  Score-normalised: the selected scores are
+         * fp32 values; their sum is taken in fp32, one rounding per addition,
+         * in j order (best first), and each weight is one fp32 division -- a
+         * definition with a single correctly rounded answer.  The softmax
+         * rules go through exp and are computed in binary64. */
         double* w = topk_w + t * k;
         if (weight_mode == ORC_W_SCORE_NORM) {
-            double den = 0.0;
-            for (int j = 0; j < k; ++j) den += cand[j].v;
-            for (int j = 0; j < k; ++j) w[j] = cand[j].v / den;
+            float den = 0.0f;
+            for (int j = 0; j < k; ++j) den = den + (float)cand[j].v;
+            for (int j = 0; j < k; ++j) w[j] = (double)((float)cand[j].v / den);
         } else if (weight_mode == ORC_W_SOFTMAX_TOPK) {
             double mx = cand[0].v, den = 0.0;
             for (int j = 0; j < k; ++j) den += exp(cand[j].v - mx);

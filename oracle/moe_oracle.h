@@ -48,18 +48,22 @@ void     orc_e4m3_from_float_array(const float* v, int64_t n, uint8_t* out);
  * q = e4m3(x / scale) with fp32 division. */
 int orc_quant_row(const uint16_t* x, int H, uint8_t* q, float* scale);
 
-/* Node-limited (grouped) top-k routing, then gate weights in binary64.
+/* Node-limited (grouped) top-k routing, then the gate weights.
  * scores [T][E] fp32; E experts in G contiguous groups (nodes) of E/G.
  * If 1 < G and kg < G: group score = the exact sum of the group's m largest
  * scores (m <= 2: exact, as a binary64 two-sum; m > 2: summed in ascending
  * order in binary64); the G - kg groups with the lowest group score are banned
  * (on equal score the higher index is banned first).
  * The k best allowed experts are taken by (score desc, index asc).
- * A NaN score ranks as -infinity.
+ * A NaN score ranks as -infinity; -0 is the score +0.
  * weight_mode: ORC_W_SOFTMAX_TOPK   softmax over the k selected scores,
- *              ORC_W_SOFTMAX_RENORM softmax over all E, renormalised over the k,
- *              ORC_W_SCORE_NORM     s_j / sum of the k selected s.
- * Outputs topk_idx [T][k] int32 and topk_w [T][k] binary64. */
+ *              ORC_W_SOFTMAX_RENORM softmax over all E, renormalised over the k
+ *                                   (both in binary64),
+ *              ORC_W_SCORE_NORM     s_j / sum of the k selected s, in fp32: the
+ *                                   sum in j order (best first), one rounding
+ *                                   per addition, then one division per weight.
+ * Outputs topk_idx [T][k] int32 and topk_w [T][k] (binary64 storage; the
+ * score-normalised weights are fp32 values). */
 int orc_route(const float* scores, int64_t T, int E, int G, int kg, int m, int k,
               int weight_mode, int32_t* topk_idx, double* topk_w);
 

@@ -114,8 +114,9 @@ def test_weights_closed_forms(orc):
     s = rng.random((64, 16)).astype(np.float32)
     idx, w = orc.route(s, 4, weight_mode=orc.W_SCORE_NORM)
     sel = np.take_along_axis(s.astype(np.float64), idx, 1)
-    assert np.allclose(w.sum(1), 1.0, rtol=0, atol=1e-15)
-    assert np.allclose(w * sel.sum(1, keepdims=True), sel, rtol=1e-15, atol=0)
+    # fp32 rule: k - 1 roundings in the sum, one per quotient
+    assert np.allclose(w.sum(1), 1.0, rtol=0, atol=8 * 2.0 ** -24)
+    assert np.allclose(w * sel.sum(1, keepdims=True), sel, rtol=8 * 2.0 ** -24, atol=0)
     # k = 2 softmax is the logistic function of the score gap
     idx, w = orc.route(s, 2, weight_mode=orc.W_SOFTMAX_TOPK)
     sel = np.take_along_axis(s.astype(np.float64), idx, 1)
@@ -146,7 +147,7 @@ def test_no_limit_nodes_formula_matches_when_groups_all_kept(orc):
     a, wa = orc.route(s, 4, num_groups=4, topk_groups=4)
     b, wb = orc.route(s, 4)
     assert np.array_equal(a, b) and np.array_equal(wa, wb)
-    assert math.isclose(float(wa.sum()), 200.0, rel_tol=1e-12)
+    assert math.isclose(float(wa.sum()), 200.0, rel_tol=8 * 2.0 ** -24)   # fp32 weights
 
 
 def test_node_scores_compare_exact_sums(orc):
@@ -175,3 +176,38 @@ def test_node_scores_compare_exact_sums(orc):
         allowed = [e for e in range(12) if e // 2 in kept]
         want = sorted(allowed, key=lambda e: (-Fraction(float(v[e])), e))[:2]
         assert idx[0].tolist() == want, (trial, v)
+
+
+def test_score_norm_weights_hand_worked(orc):
+    """Score-normalised weights on hand-worked cases (tests/golden/score_norm_weights.txt):
+    fp32 sum in j order (best first), one fp32 division per weight."""
+    from conftest import read_golden
+    rows = read_golden("score_norm_weights.txt")
+    assert len(rows) == 7
+    for r in rows:
+        s = np.array([float.fromhex(v) for v in r[0].split(",")], np.float32)[None, :]
+        want_idx = [int(v) for v in r[1].split(",")]
+        want_bits = [int(v, 16) for v in r[2].split(",")]
+        idx, w = orc.route(s, s.shape[1], weight_mode=orc.W_SCORE_NORM)
+        assert idx[0].tolist() == want_idx, r
+        got = w[0].astype(np.float32)
+        assert np.array_equal(got.astype(np.float64), w[0]), "weights are fp32 values"
+        assert got.view(np.uint32).tolist() == want_bits, (r, [hex(b) for b in got.view(np.uint32)])
+
+
+def test_score_norm_weights_sum_and_ratio(orc):
+    """Closed forms of the fp32 rule on random scores: the weights sum to 1
+    within the k-term rounding bound, w_i / w_j = s_i / s_j within two
+    roundings, and a -0 score gives the weight +0."""
+    rng = np.random.default_rng(31)
+    for k in (1, 2, 8, 16):
+        s = (rng.random((300, 32)) * 2.0 ** rng.integers(-20, 20, (300, 1))).astype(np.float32)
+        idx, w = orc.route(s, k, weight_mode=orc.W_SCORE_NORM)
+        sel = np.take_along_axis(s.astype(np.float64), idx, 1)
+        u = 2.0 ** -24
+        # sum: (k - 1) roundings in the denominator, one per quotient
+        assert np.all(np.abs(w.sum(1) - 1.0) <= 2 * k * u)
+        assert np.allclose(w / w[:, :1], sel / sel[:, :1], rtol=4 * u, atol=0)
+    s = np.array([[-0.0, -0.0, 1.0]], np.float32)
+    _, w = orc.route(s, 3, weight_mode=orc.W_SCORE_NORM)
+    assert w[0].tolist() == [1.0, 0.0, 0.0] and not np.signbit(w[0, 1:]).any()
