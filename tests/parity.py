@@ -4,9 +4,12 @@ Tolerances, derived from the arithmetic:
   - routing indices, counts, offsets, row map, receive rows, FP8 bytes and
     scales, source ids: bit-exact (integer / byte work, and the FP8 code is
     decided by one fp32 division on both sides).
-  - gate weights: the kernel computes in fp32, the oracle in binary64; u =
-    2^-24.  Score-normalised: a sum of k positive terms ((k-1) roundings)
-    and one division, within k u relative.  Softmax over the top k: each
+  - gate weights, score-normalised: bit-exact.  Both sides take the same fp32
+    definition (the sum of the selected scores in j order, one rounding per
+    addition, then one division per weight), which has one answer; NaN
+    weights (infinite or NaN scores) compare equal to NaN.
+  - gate weights, softmax rules: the kernel computes in fp32 (expf), the
+    oracle in binary64; u = 2^-24.  Softmax over the top k: each
     exp(v - max) carries the fp32 subtraction's error (at most d u in the
     exponent, d the distance of v from the maximum) and expf's (<= 2 ulp,
     4 u), in the numerator and, averaged, in the sum; then k - 1 additions
@@ -14,7 +17,7 @@ Tolerances, derived from the arithmetic:
     normaliser cancels in the ratio, leaving one more division per selected
     term, k u more.  Bound used (w_rtol): max(32, 2k + 2 (d + 4) + 2) u, d
     the largest distance between a token's best score and its selected
-    scores -- 32 u (~1.9e-6) for the workloads (k <= 8, d <= 4).
+    scores -- 32 u (~1.9e-6) for the softmax workloads (k <= 8, d <= 4).
   - combine: the kernel accumulates k fp32 fused multiply-adds and rounds once
     to bf16; the oracle sums exactly-representable products in binary64 and
     rounds once.  The fp32 error (< k * 2^-24 relative) can move the result
@@ -40,6 +43,58 @@ def w_rtol(k: int, scores: np.ndarray | None = None, idx: np.ndarray | None = No
     return max(32.0, 2 * k + 2 * (d + 4) + 2) * 2.0 ** -24
 
 
+def assert_weights_match(got: np.ndarray, want: np.ndarray, weight_mode: int, k: int,
+                         scores: np.ndarray | None = None, idx: np.ndarray | None = None):
+    """Gate weights against the oracle's: bit for bit for the score-normalised
+    rule (NaN equals NaN), within w_rtol for the softmax rules."""
+    got = np.asarray(got, np.float32)
+    if weight_mode == synth.W_SCORE_NORM:
+        want32 = np.asarray(want).astype(np.float32)
+        same = (got.view(np.uint32) == want32.view(np.uint32)) | (np.isnan(got) & np.isnan(want32))
+        bad = np.argwhere(~same)
+        assert bad.size == 0, f"weights differ at {bad[:4].tolist()}: {got[tuple(bad[0])]!r} vs {want32[tuple(bad[0])]!r}"
+    else:
+        np.testing.assert_allclose(got, want, rtol=w_rtol(k, scores, idx), atol=0)
+
+
+def assert_rows_equal(got: np.ndarray, want: np.ndarray, what: str):
+    """Element-by-element equality of two row arrays, naming the first bad row."""
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    if not np.array_equal(got, want):
+        diff = (got != want).reshape(got.shape[0], -1).any(1)
+        r = int(np.argmax(diff))
+        raise AssertionError(f"{what}: {int(diff.sum())} rows differ, first at row {r}")
+
+
+def oracle_token_payload(x_bits: np.ndarray, fp8: bool):
+    """The oracle's payload of every token, one row per token (orc_dispatch
+    with the row map t -> t): bf16 bits, or e4m3 codes [T][H] with their
+    scales [T][H/128]."""
+    import oracle
+    T = x_bits.shape[0]
+    row = np.arange(T, dtype=np.int32).reshape(T, 1)
+    q, s, _ = oracle.dispatch(x_bits, row, T, fp8)
+    return q, (s if fp8 else None)
+
+
+def oracle_identity_tokens(x_bits: np.ndarray, fp8: bool) -> np.ndarray:
+    """Each token's expert input under identity experts, oracle values only:
+    the bf16 token, or (FP8) bf16_rn(float(q) * scale) of the oracle's own
+    quantisation of it (orc_dequant_rows).  [T][H] bf16 bits."""
+    import oracle
+    q, s = oracle_token_payload(x_bits, fp8)
+    if not fp8:
+        return q
+    return oracle.dequant_rows(q, s, np.arange(x_bits.shape[0]))
+
+
+def take_rows(t: torch.Tensor, rows: np.ndarray) -> torch.Tensor:
+    """rows of a device tensor: a slice when they are 0..n-1, else a gather."""
+    if rows.size and rows[0] == 0 and rows[-1] == rows.size - 1:
+        return t[: rows.size]
+    return t.index_select(0, torch.from_numpy(np.ascontiguousarray(rows, np.int64)).to(t.device))
+
+
 def to_dev_bf16(bits: np.ndarray, dev) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
@@ -61,32 +116,3 @@ def defined_rows(w_mode: int, cnt: np.ndarray, S: int, total: int) -> np.ndarray
         return np.arange(total)
     return np.concatenate([e * S + np.arange(c) for e, c in enumerate(cnt)]) if len(cnt) else \
         np.zeros(0, np.int64)
-
-
-def dequant_on_device(q: torch.Tensor, scale: torch.Tensor, chunk: int = 8192) -> torch.Tensor:
-    """Identity expert for FP8 payloads (test harness, torch ops):
-    y = bf16(float(q) * scale) in the receive layout.  Any deterministic bf16 y
-    serves: the same y feeds the kernel and the oracle."""
-    rows, H = q.shape
-    y = torch.empty((rows, H), dtype=torch.bfloat16, device=q.device)
-    for a in range(0, rows, chunk):
-        b = min(rows, a + chunk)
-        f = q[a:b].view(torch.float8_e4m3fn).float().view(b - a, H // 128, 128)
-        f = torch.nan_to_num(f * scale[a:b, :, None], nan=0.0, posinf=0.0, neginf=0.0)
-        y[a:b] = f.view(b - a, H).to(torch.bfloat16)
-    return y
-
-
-def identity_rows(x_bits: np.ndarray, tokens, fp8: bool) -> np.ndarray:
-    """The oracle's expert input for each listed token under identity experts:
-    the token's bf16 row, or (FP8) bf16_rn(float(q) * scale) of the oracle's
-    own quantisation of it.  [len(tokens)][H] bf16 bits, oracle values only."""
-    import oracle
-    rows = []
-    for t in np.asarray(tokens).reshape(-1):
-        if fp8:
-            q, s = oracle.quant_row(x_bits[t])
-            rows.append(oracle.dequant_rows(q[None], s[None], [0])[0])
-        else:
-            rows.append(x_bits[t])
-    return np.stack(rows) if rows else np.zeros((0, x_bits.shape[1]), np.uint16)

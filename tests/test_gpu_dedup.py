@@ -21,7 +21,8 @@ import torch
 
 import oracle
 from combine_layout_gb300 import synth
-from parity import bf16_bits, bf16_ulp_diff, identity_rows, to_dev_bf16
+from parity import (assert_rows_equal, bf16_bits, bf16_ulp_diff, oracle_token_payload,
+                    to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +34,8 @@ def _ulp(bits):
     return 2.0 ** (np.floor(np.log2(np.maximum(f, 2.0 ** -126))) - 7)
 
 
-def _run(w, sample=None, x_early=False):
+def _run(w, x_early=False):
+    """The whole dedup path against the oracle, every element compared."""
     from combine_layout_gb300.pipeline import EpPipeline
     inp = synth.make_inputs(w)
     p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV,
@@ -55,73 +57,55 @@ def _run(w, sample=None, x_early=False):
     assert np.array_equal(p.drecv_src[:nd].cpu().numpy(), RL["src"])
     assert np.array_equal(p.drecv_mask[:nd].cpu().numpy().view(np.uint32), RL["mask"])
 
-    # payload of the dedup rows (sampled at full size)
-    rows = np.arange(nd)
-    if sample is not None and nd > sample:
-        rng = np.random.default_rng(11)
-        rows = np.unique(np.concatenate([rows[:64], rows[-64:], rng.choice(nd, sample)]))
-    rt = torch.from_numpy(rows).to(DEV)
-    src = RL["src"][rows]
+    # payload of every dedup row: its token's oracle payload
+    q_tok, s_tok = oracle_token_payload(inp["x"], w.fp8)
     if w.fp8:
-        q = p.drecv_x.index_select(0, rt).cpu().numpy()
-        sc = p.drecv_scale.index_select(0, rt).cpu().numpy()
-        for i, t in enumerate(src):
-            qo, so = oracle.quant_row(inp["x"][t])
-            assert np.array_equal(q[i], qo) and np.array_equal(sc[i], so), rows[i]
+        assert_rows_equal(p.drecv_x[:nd].cpu().numpy(), q_tok[RL["src"]], "dedup FP8 bytes")
+        assert_rows_equal(p.drecv_scale[:nd].cpu().numpy().view(np.uint32),
+                          s_tok[RL["src"]].view(np.uint32), "dedup FP8 scales")
     else:
-        assert np.array_equal(bf16_bits(p.drecv_x.index_select(0, rt)), inp["x"][src])
+        assert_rows_equal(bf16_bits(p.drecv_x[:nd]), q_tok[RL["src"]], "dedup bf16 payload")
 
-    # expansion = the direct dispatch's rows (oracle layout)
+    # expansion = the oracle's direct dispatch, every row
     D, _ = oracle.layout(idx_o, w.E, w.R, oracle.MODE_HT)
     nrows = int(D["off"][-1])
-    erows = np.arange(nrows)
-    if sample is not None and nrows > sample:
-        rng = np.random.default_rng(12)
-        erows = np.unique(np.concatenate([erows[:64], erows[-64:], rng.choice(nrows, sample)]))
-    want_src = np.empty(nrows, np.int64)
-    flat = D["row"].ravel()
-    want_src[flat[flat >= 0]] = np.nonzero(flat >= 0)[0] // w.k
-    et = torch.from_numpy(erows).to(DEV)
-    assert np.array_equal(p.recv_src.index_select(0, et).cpu().numpy(), want_src[erows])
+    rx_o, rs_o, src_o = oracle.dispatch(inp["x"], D["row"], nrows, w.fp8)
+    assert np.array_equal(p.recv_src[:nrows].cpu().numpy(), src_o)
     if w.fp8:
-        q = p.recv_x.index_select(0, et).cpu().numpy()
-        sc = p.recv_scale.index_select(0, et).cpu().numpy()
-        for i, t in enumerate(want_src[erows]):
-            qo, so = oracle.quant_row(inp["x"][t])
-            assert np.array_equal(q[i], qo) and np.array_equal(sc[i], so), erows[i]
+        assert_rows_equal(p.recv_x[:nrows].cpu().numpy(), rx_o, "expanded FP8 bytes")
+        assert_rows_equal(p.recv_scale[:nrows].cpu().numpy().view(np.uint32),
+                          rs_o.view(np.uint32), "expanded FP8 scales")
     else:
-        assert np.array_equal(bf16_bits(p.recv_x.index_select(0, et)), inp["x"][want_src[erows]])
+        assert_rows_equal(bf16_bits(p.recv_x[:nrows]), rx_o, "expanded bf16 payload")
 
-    # two-stage combine on the oracle's expert inputs and weights
+    # two-stage combine on the oracle's expert inputs and weights, every token
     w32 = np.ascontiguousarray(w_o, dtype=np.float32)
-    y_rows = identity_rows(inp["x"], np.arange(w.T), w.fp8)[want_src]   # [nrows][H], oracle values
+    y_tok = oracle.dequant_rows(q_tok, s_tok, np.arange(w.T)) if w.fp8 else q_tok
+    y_rows = y_tok[src_o]                                     # [nrows][H], oracle values
     y_d = torch.zeros((p.rows, w.H), dtype=torch.bfloat16, device=DEV)
     y_d[:nrows] = to_dev_bf16(y_rows, DEV)
     out = p.combine_dedup(y_d, topk_w=torch.from_numpy(w32).to(DEV))
     torch.cuda.synchronize()
-    tokens = np.arange(w.T)
-    if sample is not None and w.T > sample:
-        rng = np.random.default_rng(13)
-        tokens = np.unique(np.concatenate([tokens[:32], tokens[-32:], rng.choice(w.T, sample)]))
     want, part = oracle.combine_dedup(y_rows, idx_o, D["row"], w32, w.E, w.R, RL["drow"], nd,
-                                      tokens=tokens, want_partial=True)
-    got = bf16_bits(out[torch.from_numpy(tokens).to(DEV)])
-    qs = RL["drow"][tokens]
-    qrows = np.unique(qs[qs >= 0])
-    got_part = bf16_bits(p.partial.index_select(0, torch.from_numpy(qrows).to(DEV)))
-    dp = bf16_ulp_diff(got_part, part[qrows])
+                                      want_partial=True)
+    got = bf16_bits(out)
+    got_part = bf16_bits(p.partial[:nd])
+    dp = bf16_ulp_diff(got_part, part)
     assert dp.max() <= 1, f"partial rows differ by {dp.max()} ulp"
-    # the out bound, token by token
-    pos = {q: i for i, q in enumerate(qrows)}
-    pu = _ulp(part[qrows])
+    # the out bound, every token: the sum of its partials' ulps plus the
+    # result's; where all its partials agree, 1 ulp
+    qs = RL["drow"]
+    pu = _ulp(part)
     g = synth.bf16_bits_to_f32(got).astype(np.float64)
     o = synth.bf16_bits_to_f32(want).astype(np.float64)
-    for i, t in enumerate(tokens):
-        mine = [pos[q] for q in qs[i] if q >= 0]
-        bound = pu[mine].sum(0) + np.maximum(_ulp(got[i]), _ulp(want[i]))
-        assert np.all(np.abs(g[i] - o[i]) <= bound * (1 + 1e-6)), t
-        if np.all(dp[mine] == 0):
-            assert bf16_ulp_diff(got[i], want[i]).max() <= 1, t
+    bound = np.maximum(_ulp(got), _ulp(want))
+    agree = np.ones(w.T, bool)
+    for j in range(w.k):
+        has = qs[:, j] >= 0
+        bound[has] += pu[qs[has, j]]
+        agree[has] &= dp[qs[has, j]].max(1) == 0
+    assert np.all(np.abs(g - o) <= bound * (1 + 1e-6)), "out outside the two-rounding bound"
+    assert bf16_ulp_diff(got[agree], want[agree]).max(initial=0) <= 1
     p.close()
     return nd, nrows
 
@@ -137,10 +121,11 @@ def test_dedup_elementwise(name, T):
         assert nd == nrows                    # one expert per rank: nothing to dedup
 
 
-@pytest.mark.parametrize("name", ["ht_prefill", "ht_prefill_fp8"])
+@pytest.mark.parametrize("name", ["ht_prefill", "ht_prefill_fp8", "skewed", "mixtral"])
 def test_dedup_full_size(name):
-    nd, nrows = _run(synth.WORKLOADS[name], sample=1024)
-    assert nd < nrows
+    w = synth.WORKLOADS[name]
+    nd, nrows = _run(w)
+    assert nd < nrows if w.E // w.R > 1 else nd == nrows
 
 
 @pytest.mark.parametrize("name", ["ht_prefill", "ht_prefill_fp8"])

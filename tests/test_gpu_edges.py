@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from combine_layout_gb300 import synth
-from parity import bf16_bits, bf16_ulp_diff, to_dev_bf16
+from parity import assert_weights_match, bf16_bits, bf16_ulp_diff, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -229,10 +229,12 @@ def test_router_adversarial_scores(E, G, kg, k, m):
     p = EpPipeline(synth.MODE_HT, E, E // 8 if E >= 8 else 1, T, 128, k, device=DEV)
     p.route(torch.from_numpy(s).to(DEV), T, G, kg, m, synth.W_SCORE_NORM)
     torch.cuda.synchronize()
-    idx_o, _ = oracle.route(s, k, G, kg, group_topk=m, weight_mode=oracle.W_SCORE_NORM)
+    idx_o, w_o = oracle.route(s, k, G, kg, group_topk=m, weight_mode=oracle.W_SCORE_NORM)
     got = p.topk_idx[:T].cpu().numpy()
     bad = np.nonzero((got != idx_o).any(1))[0]
     assert bad.size == 0, (bad[:5], got[bad[:2]], idx_o[bad[:2]])
+    # score-normalised weights, bit for bit (infinite and NaN sums included)
+    assert_weights_match(p.topk_w[:T].cpu().numpy(), w_o, synth.W_SCORE_NORM, k)
     p.close()
 
 

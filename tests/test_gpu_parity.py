@@ -1,12 +1,13 @@
 """GPU parity: libmoeep (through the C ABI) against the CPU oracle on the same
 seeded inputs, for the five workloads.
 
-Reduced token counts (several 32-token tiles plus a ragged tail) are compared
-element by element; the full-size workloads, in the launch configuration the
+Every case compares every output element: routing, gate weights, layout,
+every receive row the layout defines (bf16 payload, or FP8 bytes and scales,
+and the source token), and every combined token.  Reduced token counts
+(several 32-token tiles plus a ragged tail) and the full-size workloads run
+the same comparison; the full sizes in the launch configuration the
 benchmark times (including its moe_ep_set_x_before_route declaration, in
-test_parity_with_x_before_route), compare routing and layout in full and
-dispatch / combine on sampled rows and tokens the oracle computes one by one.  Tolerances: see
-tests/parity.py.
+test_parity_with_x_before_route).  Tolerances: see tests/parity.py.
 """
 from __future__ import annotations
 
@@ -16,8 +17,8 @@ import torch
 
 import oracle
 from combine_layout_gb300 import synth
-from parity import (bf16_bits, bf16_ulp_diff, defined_rows, dequant_on_device,
-                    identity_rows, to_dev_bf16, w_rtol)
+from parity import (assert_rows_equal, assert_weights_match, bf16_bits, bf16_ulp_diff,
+                    defined_rows, oracle_identity_tokens, take_rows, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +36,7 @@ def _check_route_layout(w, p, inp):
     wg = p.topk_w[: w.T].cpu().numpy()
     idx_o, w_o = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
     assert np.array_equal(idx, idx_o), "topk_idx differs"
-    np.testing.assert_allclose(wg, w_o, rtol=w_rtol(w.k, inp["scores"], idx_o), atol=0)
+    assert_weights_match(wg, w_o, w.weight_mode, w.k, inp["scores"], idx_o)
     L = {k: v.cpu().numpy() for k, v in p.layout().items()}
     L_o, st = oracle.layout(idx_o, w.E, w.R, w.mode, w.slots)
     assert st == oracle.OK
@@ -44,7 +45,7 @@ def _check_route_layout(w, p, inp):
     return idx_o, w_o, L_o
 
 
-def _run(w, sample=None, seed=None, x_early=False):
+def _run(w, seed=None, x_early=False):
     inp = synth.make_inputs(w, seed)
     p = _pipeline(w, x_early)
     scores = torch.from_numpy(inp["scores"]).to(DEV)
@@ -62,53 +63,35 @@ def _run(w, sample=None, seed=None, x_early=False):
         assert total == w.E * w.slots
     assert np.array_equal(p.recv_cnt.cpu().numpy(), L_o["cnt"])
 
+    # the oracle's dispatch of every pair into the receive layout; every
+    # defined row is compared
+    rx_o, rs_o, src_o = oracle.dispatch(inp["x"], L_o["row"], p.rows, w.fp8)
     rows = defined_rows(w.mode, L_o["cnt"], w.slots, int(L_o["off"][-1]))
-    if sample is not None and rows.size > sample:
-        rng = np.random.default_rng(123)
-        rows = np.unique(np.concatenate([rows[:64], rows[-64:], rng.choice(rows, sample)]))
-    src = p.recv_src.cpu().numpy()[rows]
-    # where every pair's token lands, by the oracle's layout
-    want_src = np.empty(p.rows, np.int64)
-    flat = L_o["row"].ravel()
-    ok = flat >= 0
-    want_src[flat[ok]] = np.nonzero(ok)[0] // w.k
-    assert np.array_equal(src, want_src[rows]), "recv_src differs"
-
-    rows_t = torch.from_numpy(rows).to(DEV)
+    assert np.array_equal(take_rows(p.recv_src, rows).cpu().numpy(), src_o[rows]), "recv_src"
     if w.fp8:
-        q = p.recv_x.index_select(0, rows_t).cpu().numpy()
-        sc = p.recv_scale.index_select(0, rows_t).cpu().numpy()
-        for i, t in enumerate(want_src[rows]):
-            qo, so = oracle.quant_row(inp["x"][t])
-            assert np.array_equal(q[i], qo), f"FP8 bytes differ at row {rows[i]}"
-            assert np.array_equal(sc[i], so), f"scales differ at row {rows[i]}"
-        y = dequant_on_device(p.recv_x, p.recv_scale)
+        assert_rows_equal(take_rows(p.recv_x, rows).cpu().numpy(), rx_o[rows], "FP8 bytes")
+        assert_rows_equal(take_rows(p.recv_scale, rows).cpu().numpy().view(np.uint32),
+                          rs_o[rows].view(np.uint32), "FP8 scales")
+        # expert input: each row's token dequantised by the oracle (identity
+        # experts); the same y feeds the kernel and the oracle
+        y_o = np.zeros((p.rows, w.H), np.uint16)
+        y_o[rows] = oracle_identity_tokens(inp["x"], True)[src_o[rows]]
+        y = to_dev_bf16(y_o, DEV)
     else:
-        got = bf16_bits(p.recv_x.index_select(0, rows_t))
-        assert np.array_equal(got, inp["x"][want_src[rows]]), "bf16 payload differs"
-        y = p.recv_x
+        assert_rows_equal(bf16_bits(take_rows(p.recv_x, rows)), rx_o[rows], "bf16 payload")
+        y_o, y = rx_o, p.recv_x
 
-    # both sides combine with the oracle's gate weights (fp32)
-    w32 = np.zeros((w.T, w.k), np.float32)
-    w32[:] = w_o
+    # both sides combine with the oracle's gate weights (fp32), every token
+    w32 = np.ascontiguousarray(w_o, dtype=np.float32)
     out = p.combine(y, topk_w=torch.from_numpy(w32).to(DEV))
     torch.cuda.synchronize()
-    tokens = np.arange(w.T)
-    if sample is not None and w.T > sample:
-        rng = np.random.default_rng(7)
-        tokens = np.unique(np.concatenate([tokens[:32], tokens[-32:], rng.choice(w.T, sample)]))
-    # the oracle's own expert input for every pair of these tokens (identity
-    # experts: the token, or its FP8 round trip), rows compacted
-    r = L_o["row"][tokens]
-    y_c = np.repeat(identity_rows(inp["x"], tokens, w.fp8), w.k, axis=0)
-    row_c = np.where(r.ravel() >= 0, np.arange(r.size), -1).reshape(r.shape).astype(np.int32)
-    want = oracle.combine(y_c, row_c, w32[tokens])
-    got = bf16_bits(out[torch.from_numpy(tokens).to(DEV)])
+    want = oracle.combine(y_o, L_o["row"], w32)
+    got = bf16_bits(out)
     d = bf16_ulp_diff(got, want)
     assert d.max() <= 1, f"combine differs by {d.max()} bf16 ulp"
     # round trip: identity experts, weights summing to 1, bf16 payload -> x within 1 ulp
     if not w.fp8:
-        rt = bf16_ulp_diff(got, inp["x"][tokens])
+        rt = bf16_ulp_diff(got, inp["x"])
         assert rt.max() <= 1, f"round trip off by {rt.max()} ulp"
     p.close()
     return d
@@ -125,13 +108,14 @@ def test_parity_elementwise(name, T):
 @pytest.mark.parametrize("name", ["tiny_ll", "ll_decode", "ht_prefill", "ht_prefill_fp8",
                                   "mixtral", "skewed"])
 def test_parity_full_size(name):
-    _run(synth.WORKLOADS[name], sample=1024)
+    _run(synth.WORKLOADS[name])
 
 
 @pytest.mark.parametrize("name,T,H", [("tiny_ll", 77, None), ("ll_decode", 128, None),
                                       ("ht_prefill", 300, None), ("ht_prefill_fp8", 300, None),
                                       ("ht_prefill_fp8", 300, 640), ("mixtral", 1000, None),
-                                      ("ht_prefill", 4096, None), ("ht_prefill_fp8", 4096, None)])
+                                      ("ht_prefill", 4096, None), ("ht_prefill_fp8", 4096, None),
+                                      ("mixtral", 8192, None)])
 def test_parity_with_x_before_route(name, T, H):
     """moe_ep_set_x_before_route: each bf16 dispatch CTA reads its token
     before waiting for the router; the results are the same (the FP8 cases,
@@ -143,7 +127,7 @@ def test_parity_with_x_before_route(name, T, H):
         d.pop("extra")
         d["H"] = H
         w = synth.Workload(**d)
-    _run(w, sample=1024 if T > 1000 else None, x_early=True)
+    _run(w, x_early=True)
 
 
 def test_fp8_conversion_sweep_all_bf16_values():

@@ -6,8 +6,8 @@ workspace is allocated.  This entry point keeps its scratch in a static device
 array instead.  The test calls it through the C ABI twice in a row and checks
 each result against the handle-based entry points (moe_ep_route followed by
 moe_ep_copy_layout) on the same inputs: routing, counts, offsets and the row
-map bit for bit, gate weights within the parity tests' tolerance.  It lives in
-a file of its own that pytest collects last.
+map and gate weights bit for bit (both run the same router).  It lives in a
+file of its own that pytest collects last.
 """
 from __future__ import annotations
 
@@ -16,7 +16,6 @@ import pytest
 import torch
 
 from combine_layout_gb300 import synth
-from parity import W_RTOL
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +48,7 @@ def _both(w, seed):
     got = {k_: v.cpu().numpy() for k_, v in out.items()}
     for key in ("idx", "row", "cnt", "off", "rcnt", "roff"):
         assert np.array_equal(got[key], ref[key]), key
-    np.testing.assert_allclose(got["w"], ref["w"], rtol=W_RTOL, atol=0)
+    assert np.array_equal(got["w"].view(np.uint32), ref["w"].view(np.uint32)), "w"
 
 
 def test_static_entry_point_matches_handle_path_twice_in_a_row():
@@ -59,9 +58,16 @@ def test_static_entry_point_matches_handle_path_twice_in_a_row():
     _both(synth.WORKLOADS["tiny_ll"].with_tokens(77, slots=128), seed=13)
 
 
-def test_static_entry_point_rejects_sizes_beyond_its_scratch():
+def test_static_entry_point_at_its_capacity():
+    # ceil(8192 / 32) * 256 = 65536 cells: exactly the scratch's capacity,
+    # where the last group of byte counts is padded the most
+    _both(synth.WORKLOADS["ht_prefill"].with_tokens(8192), seed=14)
+
+
+@pytest.mark.parametrize("T", [8193, 16384])
+def test_static_entry_point_rejects_sizes_beyond_its_scratch(T):
     import combine_layout_gb300.moe_ep as ep
-    T, E = 16384, 256            # 512 tiles x 256 experts > 65536 cells
+    E = 256                      # 257 or 512 tiles x 256 experts > 65536 cells
     z = torch.zeros((T, E), device=DEV)
     i32 = dict(dtype=torch.int32, device=DEV)
     with pytest.raises(ep.MoeEpError) as e:
