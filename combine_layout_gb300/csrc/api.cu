@@ -65,8 +65,13 @@ struct moe_ep_handle {
     int64_t host_total;   // total rows known on the host (-1: not queried)
     int align;            // HT expert blocks padded to a multiple of align rows
     int x_early;          // x is complete before the route (moe_ep_set_x_before_route)
-    cudaEvent_t sent;     // recorded after a send-only dispatch / combine
-    int has_sent;
+    // send-only operations (staged execution): the send kernels' CTA arrival
+    // counter and the signal their last CTA adds 1 to (device workspace), the
+    // event recorded after the last send, and the sends not yet completed
+    unsigned* send_arrive;
+    unsigned* send_signal;
+    cudaEvent_t sent;
+    unsigned pending;
 };
 
 namespace {
@@ -74,6 +79,12 @@ namespace {
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_EP_OK : MOE_EP_ERR_CUDA; }
+
+// Limit of the receive wait that moe_ep_complete enqueues: its sends are
+// ordered before it, so in correct use the first poll succeeds.
+constexpr uint64_t kCompleteWaitNs = 200ull * 1000 * 1000;
+// Largest limit moe_ep_wait_signal accepts.
+constexpr int64_t kMaxWaitNs = 10ll * 1000 * 1000 * 1000;
 
 inline int check_group(const moe_ep_group* g)
 {
@@ -257,12 +268,12 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     const size_t ntn = (size_t)h->ntiles_max * g->R;
     const size_t cstride = ((size_t)h->ntiles_max + 15) / 16 * 16;
     const size_t ngrp = cstride / 16;
-    const size_t counts[21] = {nt, ngrp * g->E, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
+    const size_t counts[23] = {nt, ngrp * g->E, (size_t)g->E, (size_t)g->E + 1, (size_t)g->R,
                                (size_t)g->R + 1, (size_t)g->S * max_topk, (size_t)g->S * max_topk, 1,
                                (size_t)g->E * cstride / 4,
                                ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1,
                                ntn, (size_t)g->R * cstride / 4, ngrp * g->R, 1, (size_t)g->R,
-                               (size_t)g->R + 1, (size_t)g->S * max_topk};
+                               (size_t)g->R + 1, (size_t)g->S * max_topk, 1, 1};
     size_t bytes = 0;
     for (size_t c : counts) bytes += (sizeof(int32_t) * c + 255) & ~(size_t)255;
     void* base = nullptr;
@@ -292,6 +303,8 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->rk_cnt = carve<int32_t>(cur, counts[18]);
     h->rk_off = carve<int32_t>(cur, counts[19]);
     h->drow = carve<int32_t>(cur, counts[20]);
+    h->send_arrive = carve<unsigned>(cur, 1);
+    h->send_signal = carve<unsigned>(cur, 1);
     if (cudaMemset(base, 0, bytes) != cudaSuccess) {
         cudaFree(base);
         delete h;
@@ -321,7 +334,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
         delete h;
         return MOE_EP_ERR_CUDA;
     }
-    h->has_sent = 0;
+    h->pending = 0;
     h->routed = 0;
     h->rows_ready = 0;
     h->words_only = 0;
@@ -473,9 +486,14 @@ int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_r
     return MOE_EP_OK;
 }
 
-int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, float* recv_scale,
-                    int32_t* recv_src, int32_t* recv_cnt, int64_t recv_rows,
-                    moe_ep_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+// moe_ep_dispatch, and with sig the send of moe_ep_dispatch_send.
+int dispatch_impl(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, float* recv_scale,
+                  int32_t* recv_src, int32_t* recv_cnt, int64_t recv_rows, cudaStream_t stream,
+                  const SendSignal& sig)
 {
     if (!h) return MOE_EP_ERR_INVALID;
     moe_ep_group* g = h->g;
@@ -492,10 +510,11 @@ int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, flo
     if (recv_src && ((uintptr_t)recv_src & 3u)) return MOE_EP_ERR_INVALID;
     if (recv_cnt && ((uintptr_t)recv_cnt & 3u)) return MOE_EP_ERR_INVALID;
     LayoutArgs fin = layout_args(h, h->T);
-    st = cuda_status(launch_dispatch(row_args(h), x, g->H, fp8, h->row, recv_x, recv_scale,
-                                     recv_src, h->cnt, recv_cnt, g->sm_count,
-                                     (cudaStream_t)stream, h->layout_pending ? &fin : nullptr,
-                                     h->x_early));
+    RowArgs ra = row_args(h);
+    ra.sig = sig;
+    st = cuda_status(launch_dispatch(ra, x, g->H, fp8, h->row, recv_x, recv_scale, recv_src,
+                                     h->cnt, recv_cnt, g->sm_count, stream,
+                                     h->layout_pending ? &fin : nullptr, h->x_early));
     if (st == MOE_EP_OK) {
         h->rows_ready = 1;
         h->layout_pending = 0;
@@ -503,8 +522,9 @@ int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, flo
     return st;
 }
 
-int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
-                   int64_t recv_rows, moe_ep_stream_t stream)
+// moe_ep_combine, and with sig the send of moe_ep_combine_send.
+int combine_impl(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
+                 int64_t recv_rows, cudaStream_t stream, const SendSignal& sig)
 {
     if (!h) return MOE_EP_ERR_INVALID;
     moe_ep_group* g = h->g;
@@ -522,32 +542,71 @@ int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* 
         const char* oe = ob + (size_t)h->T * g->H * 2;
         if (ob < ye && yb < oe) return MOE_EP_ERR_INVALID;
     }
-    st = ensure_rows(h, (cudaStream_t)stream);
+    st = ensure_rows(h, stream);
     if (st != MOE_EP_OK) return st;
     return cuda_status(launch_combine(y, h->T, g->H, h->k, h->row, topk_w, out, g->sm_count,
-                                      (cudaStream_t)stream));
+                                      stream, sig));
+}
+
+// The send kernels of one handle run in issue order: a send waits (on the
+// device) for the handle's previous send, wherever it was enqueued.
+int before_send(moe_ep_handle_t h, cudaStream_t send_stream, SendSignal* sig)
+{
+    if (!h) return MOE_EP_ERR_INVALID;
+    int st = check_group(h->g);
+    if (st != MOE_EP_OK) return st;
+    if (h->pending && cudaStreamWaitEvent(send_stream, h->sent, 0) != cudaSuccess)
+        return MOE_EP_ERR_CUDA;
+    sig->arrive = h->send_arrive;
+    sig->signal = h->send_signal;
+    return MOE_EP_OK;
+}
+
+int after_send(moe_ep_handle_t h, cudaStream_t send_stream)
+{
+    if (cudaEventRecord(h->sent, send_stream) != cudaSuccess) return MOE_EP_ERR_CUDA;
+    h->pending += 1;
+    return MOE_EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_ep_dispatch(moe_ep_handle_t h, const void* x, int fp8, void* recv_x, float* recv_scale,
+                    int32_t* recv_src, int32_t* recv_cnt, int64_t recv_rows,
+                    moe_ep_stream_t stream)
+{
+    return dispatch_impl(h, x, fp8, recv_x, recv_scale, recv_src, recv_cnt, recv_rows,
+                         (cudaStream_t)stream, SendSignal{});
+}
+
+int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
+                   int64_t recv_rows, moe_ep_stream_t stream)
+{
+    return combine_impl(h, y, topk_w, out, recv_rows, (cudaStream_t)stream, SendSignal{});
 }
 
 int moe_ep_dispatch_send(moe_ep_handle_t h, const void* x, int fp8, void* recv_x,
                          float* recv_scale, int32_t* recv_src, int32_t* recv_cnt,
                          int64_t recv_rows, moe_ep_stream_t send_stream)
 {
-    int st = moe_ep_dispatch(h, x, fp8, recv_x, recv_scale, recv_src, recv_cnt, recv_rows,
-                             send_stream);
-    if (st != MOE_EP_OK) return st;
-    if (cudaEventRecord(h->sent, (cudaStream_t)send_stream) != cudaSuccess) return MOE_EP_ERR_CUDA;
-    h->has_sent = 1;
-    return MOE_EP_OK;
+    SendSignal sig;
+    cudaStream_t s = (cudaStream_t)send_stream;
+    int st = before_send(h, s, &sig);
+    if (st == MOE_EP_OK)
+        st = dispatch_impl(h, x, fp8, recv_x, recv_scale, recv_src, recv_cnt, recv_rows, s, sig);
+    return st == MOE_EP_OK ? after_send(h, s) : st;
 }
 
 int moe_ep_combine_send(moe_ep_handle_t h, const void* y, const float* topk_w, void* out,
                         int64_t recv_rows, moe_ep_stream_t send_stream)
 {
-    int st = moe_ep_combine(h, y, topk_w, out, recv_rows, send_stream);
-    if (st != MOE_EP_OK) return st;
-    if (cudaEventRecord(h->sent, (cudaStream_t)send_stream) != cudaSuccess) return MOE_EP_ERR_CUDA;
-    h->has_sent = 1;
-    return MOE_EP_OK;
+    SendSignal sig;
+    cudaStream_t s = (cudaStream_t)send_stream;
+    int st = before_send(h, s, &sig);
+    if (st == MOE_EP_OK) st = combine_impl(h, y, topk_w, out, recv_rows, s, sig);
+    return st == MOE_EP_OK ? after_send(h, s) : st;
 }
 
 int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream)
@@ -555,8 +614,34 @@ int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream)
     if (!h) return MOE_EP_ERR_INVALID;
     int st = check_group(h->g);
     if (st != MOE_EP_OK) return st;
-    if (!h->has_sent) return MOE_EP_OK;
-    return cuda_status(cudaStreamWaitEvent((cudaStream_t)stream, h->sent, 0));
+    if (!h->pending) return MOE_EP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    // order the receive after the sends (no kernel waits for one that may not
+    // be running), then check on the device that every send has signalled
+    if (cudaStreamWaitEvent(s, h->sent, 0) != cudaSuccess) return MOE_EP_ERR_CUDA;
+    st = cuda_status(launch_wait_signal(h->send_signal, h->pending, kCompleteWaitNs,
+                                        h->g->err_dev, s));
+    if (st == MOE_EP_OK) h->pending = 0;
+    return st;
+}
+
+int moe_ep_signal_add(moe_ep_group_t g, uint32_t* signal, uint32_t value, moe_ep_stream_t stream)
+{
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!signal || ((uintptr_t)signal & 3u)) return MOE_EP_ERR_INVALID;
+    return cuda_status(launch_signal_add(signal, value, (cudaStream_t)stream));
+}
+
+int moe_ep_wait_signal(moe_ep_group_t g, uint32_t* signal, uint32_t expected, int64_t timeout_ns,
+                       moe_ep_stream_t stream)
+{
+    int st = check_group(g);
+    if (st != MOE_EP_OK) return st;
+    if (!signal || ((uintptr_t)signal & 3u) || timeout_ns <= 0 || timeout_ns > kMaxWaitNs)
+        return MOE_EP_ERR_INVALID;
+    return cuda_status(launch_wait_signal(signal, expected, (uint64_t)timeout_ns, g->err_dev,
+                                          (cudaStream_t)stream));
 }
 
 int moe_ep_set_row_align(moe_ep_handle_t h, int align)

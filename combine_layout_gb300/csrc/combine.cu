@@ -35,7 +35,8 @@ constexpr int combine_min_ctas(int kmax)
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kernel(
     const uint4* __restrict__ y, int T, int k, int nvec, int nsplit,
-    const int32_t* __restrict__ row, const float* __restrict__ w, uint4* __restrict__ out)
+    const int32_t* __restrict__ row, const float* __restrict__ w, uint4* __restrict__ out,
+    SendSignal sig)
 {
     griddep_wait();
     __shared__ int s_row[KMAX];
@@ -68,25 +69,29 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
         }
         __syncthreads();
     }
+    send_arrive(sig);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,
-                           void* out, int sm_count, cudaStream_t s)
+                           void* out, int sm_count, cudaStream_t s, const SendSignal& sig)
 {
-    if (T <= 0) return cudaSuccess;
+    if (T <= 0 && !sig.signal) return cudaSuccess;
+    if (T < 0) T = 0;
     const int nvec = H / 8;
     // one CTA per token (or per token slice in small batches), at most 16
-    // per SM (grid-stride beyond: small tokens then amortise the CTA launch)
-    const int nsplit = (nvec % 16 == 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    // per SM (grid-stride beyond: small tokens then amortise the CTA launch);
+    // a send-only launch with no tokens still runs one CTA, for the signal
+    const int nsplit = (nvec % 16 == 0 && T > 0) ? slices_for(T, nvec / 16, sm_count) : 1;
     const int items = T * nsplit;
-    const int blocks = items < sm_count * 16 ? items : sm_count * 16;
+    int blocks = items < sm_count * 16 ? items : sm_count * 16;
+    if (blocks < 1) blocks = 1;
     const uint4* yy = (const uint4*)y;
     uint4* oo = (uint4*)out;
 #define MOEEP_COMBINE(KM)                                                                      \
     return launch_pdl(combine_kernel<KM>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,     \
-                      nsplit, row, w, oo)
+                      nsplit, row, w, oo, sig)
     if (k <= 1) MOEEP_COMBINE(1);
     if (k <= 2) MOEEP_COMBINE(2);
     if (k <= 4) MOEEP_COMBINE(4);

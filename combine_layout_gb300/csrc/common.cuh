@@ -70,6 +70,41 @@ __device__ __forceinline__ void griddep_launch_dependents()
 }
 #endif
 
+// Completion signal of a send-only dispatch or combine ("NCCL EP 论文解读",
+// item "send_only与双buffer": the send and the receive are separate kernels).
+// arrive counts the CTAs of the send kernel that have finished (the last one
+// resets it to 0); signal counts the sends that have landed and that no
+// receive has consumed yet.  Both null: not a send-only launch.
+struct SendSignal {
+    unsigned* arrive = nullptr;
+    unsigned* signal = nullptr;
+};
+
+#ifdef __CUDACC__
+// Called once by every CTA of a send kernel, with all its threads, after its
+// last store.  The barrier orders the CTA's stores before thread 0's arrival
+// (an atomic add with acquire-release semantics at GPU scope); the last CTA
+// to arrive has acquired every other CTA's stores and publishes them all
+// with its release add on the signal.
+__device__ __forceinline__ void send_arrive(const SendSignal& sig)
+{
+    if (!sig.signal) return;  // uniform across the grid
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(sig.arrive)
+                     : "memory");
+        if (prev == gridDim.x - 1) {
+            // the next send kernel starts after this grid has completed
+            *sig.arrive = 0u;
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sig.signal) : "memory");
+        }
+    }
+}
+#endif
+
 struct RouteParams {
     int E;      // experts
     int G;      // routing groups (nodes)
@@ -134,6 +169,7 @@ struct RowArgs {
     uint32_t* mask;            // G > 1: per row, bit l = local expert l of the token (may be null)
     int32_t* off_out;          // dispatch: copy of off[0 .. ncols] (may be null)
     int from_words = 0;        // 1: rank pairs from the tile words alone (deferred LL layout)
+    SendSignal sig;            // dispatch: set for a send-only launch
 };
 
 // What the receiver side of the per-rank dedup path needs: the expert layout
@@ -221,7 +257,19 @@ cudaError_t launch_combine_partial(const RowArgs& ex, const int32_t* row, const 
                                    int sm_count, cudaStream_t s);
 
 // Combine: out[t] = bf16(sum_j w[t][j] * y[row[t][j]]) (w == nullptr: weights 1).
+// sig: set for a send-only launch (then a grid is launched even for T = 0, so
+// the signal still arrives).
 cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* row, const float* w,
-                           void* out, int sm_count, cudaStream_t s);
+                           void* out, int sm_count, cudaStream_t s,
+                           const SendSignal& sig = SendSignal{});
+
+// Receive side of a send-only operation: one thread waits (at most limit_ns,
+// and a bounded number of polls) until *signal >= expected, then subtracts
+// expected; when the bound passes first it latches err[kErrTimeout].
+cudaError_t launch_wait_signal(uint32_t* signal, uint32_t expected, uint64_t limit_ns,
+                               unsigned* err, cudaStream_t s);
+// *signal += value with release semantics at GPU scope, after the work before
+// it on the stream.
+cudaError_t launch_signal_add(uint32_t* signal, uint32_t value, cudaStream_t s);
 
 }  // namespace moeep

@@ -111,7 +111,10 @@ __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
     if (early && item) load(vb);
     griddep_wait();
     if (blockIdx.x == 0) copy_counts<NT>(ra, cnt, recv_cnt, fin);
-    if (!item) return;
+    if (!item) {
+        send_arrive(ra.sig);
+        return;
+    }
     if (!early) load(vb);
     place_token(ra, t, row, recv_src, s_row, sl == 0);
     __syncthreads();
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
         load(pass);
         store(pass);
     }
+    send_arrive(ra.sig);
 }
 
 // FP8 e4m3 of one 16-byte vector of eight bf16 values; a half-warp (16 lanes
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(
         }
         __syncthreads();
     }
+    send_arrive(ra.sig);
 }
 
 // FP8 dispatch for slices of exactly NV * 128 vectors (a row of
@@ -277,6 +282,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_fit_kernel(
         }
         __syncthreads();
     }
+    send_arrive(ra.sig);
 }
 
 }  // namespace

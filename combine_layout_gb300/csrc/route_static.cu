@@ -39,7 +39,9 @@ std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array for the current device, looked up once
-// per device (with that device current) and then reused.
+// per device (with that device current) and then reused for the life of the
+// process: it belongs to the device's primary context, so it is stale after
+// cudaDeviceReset (the header tells callers not to use the entry point then).
 int scratch_for_current_device(unsigned char** out)
 {
     int dev = -1;

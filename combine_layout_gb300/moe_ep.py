@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "moe_ep_dispatch_send": [P, P, I, P, P, P, P, I64, P],
         "moe_ep_combine_send": [P, P, P, P, I64, P],
         "moe_ep_complete": [P, P],
+        "moe_ep_signal_add": [P, P, ctypes.c_uint32, P],
+        "moe_ep_wait_signal": [P, P, ctypes.c_uint32, I64, P],
         "moe_ep_dequant": [P, P, P, P, I64, P],
         "moe_ep_route_layout_static": [P, I, I, I, I, I, ctypes.POINTER(RouteOpts), P, P, P, P, P,
                                        P, P, P],
@@ -204,6 +206,17 @@ def moe_ep_combine_send(handle: int, y, topk_w, out, recv_rows: int | None = Non
 
 def moe_ep_complete(handle: int, stream=None) -> None:
     _check("moe_ep_complete", _lib.moe_ep_complete(ctypes.c_void_p(handle), _stream(stream)))
+
+
+def moe_ep_signal_add(group: int, signal, value: int, stream=None) -> None:
+    """signal: a one-element uint32 / int32 device tensor."""
+    _check("moe_ep_signal_add", _lib.moe_ep_signal_add(ctypes.c_void_p(group), _ptr(signal),
+                                                       value, _stream(stream)))
+
+
+def moe_ep_wait_signal(group: int, signal, expected: int, timeout_ns: int, stream=None) -> None:
+    _check("moe_ep_wait_signal", _lib.moe_ep_wait_signal(ctypes.c_void_p(group), _ptr(signal),
+                                                         expected, timeout_ns, _stream(stream)))
 
 
 def moe_ep_set_row_align(handle: int, align: int) -> None:

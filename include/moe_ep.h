@@ -29,8 +29,10 @@
  *    synchronisation once the kernel has finished; while it is set every call
  *    on the group returns MOE_EP_ERR_DEVICE (MOE_EP_ERR_TIMEOUT when a
  *    bounded wait gave up) until moe_ep_clear_device_errors.
- *    Kernels never trap and never wait on another kernel; the only waits are
- *    on a CTA's own bulk copies, each bounded.
+ *    Kernels never trap and never wait on a kernel that may still be
+ *    running: the only waits are on a CTA's own bulk copies and on signal
+ *    words whose producers are ordered before the waiting kernel, each
+ *    bounded.
  *  - A handle's workspace is reused by each moe_ep_route call: use one handle
  *    per forward pass in flight (for instance one per layer).
  */
@@ -193,19 +195,49 @@ MOE_EP_API int moe_ep_combine(moe_ep_handle_t h, const void* y, const float* top
  * two handles -- double buffers -- overlap one's transfer with the other's
  * expert computation; "低延迟模式" on the DeepEP page: the LL hook).
  * moe_ep_dispatch_send / moe_ep_combine_send: the same work as moe_ep_dispatch
- * / moe_ep_combine, enqueued on `send_stream`, after which the handle records
- * its completion event.  moe_ep_complete: makes `stream` wait (on the device,
- * no host synchronisation) until the handle's last send-only operation has
- * finished; a no-op if the handle never sent.  On one GPU the data lands in
- * the receive rows when the send kernel ends, so completion is that kernel's
- * end; no kernel ever spins.  With LL mode (no host synchronisation anywhere)
- * route, sends, completes and combines can be captured into a CUDA graph. */
+ * / moe_ep_combine, enqueued on `send_stream`; the send kernel's last CTA, once
+ * every CTA's stores are done, adds 1 to the handle's device signal word
+ * ("设备API GIN": SignalAdd), and the handle records an event after it.  A
+ * handle's sends run in issue order (each waits, on the device, for the
+ * previous one).  moe_ep_complete: the receive -- makes `stream` wait (on the
+ * device, no host synchronisation) for the handle's last send, then enqueues a
+ * one-thread kernel that checks the signal word holds the number of sends
+ * since the last complete and takes that number off it ("WaitOnSignal"), so
+ * the word is ready for the next micro-batch, also across CUDA-graph replays.
+ * Because of the event join the check's first poll succeeds in correct use;
+ * its wait is bounded (200 ms): if the signal is short it latches
+ * MOE_EP_DEVERR_TIMEOUT and the group's next call returns MOE_EP_ERR_TIMEOUT.
+ * A no-op if the handle has no send since its last complete.  With LL mode
+ * (no host synchronisation anywhere) route, sends, completes and combines can
+ * be captured into a CUDA graph (capture the sends and their complete in the
+ * same graph). */
 MOE_EP_API int moe_ep_dispatch_send(moe_ep_handle_t h, const void* x, int fp8, void* recv_x,
                                     float* recv_scale, int32_t* recv_src, int32_t* recv_cnt,
                                     int64_t recv_rows, moe_ep_stream_t send_stream);
 MOE_EP_API int moe_ep_combine_send(moe_ep_handle_t h, const void* y, const float* topk_w,
                                    void* out, int64_t recv_rows, moe_ep_stream_t send_stream);
 MOE_EP_API int moe_ep_complete(moe_ep_handle_t h, moe_ep_stream_t stream);
+
+/* Device signal words ("NCCL EP 论文解读", item "设备API GIN": SignalAdd adds to a
+ * signal word, WaitOnSignal waits until it reaches an expected value) -- the
+ * primitives under moe_ep_complete, for a caller's own producers and consumers.
+ * signal: device uint32 (4-byte aligned), owned by the caller, starting at 0.
+ * moe_ep_signal_add: after the work before it on `stream`, *signal += value
+ * with release semantics at GPU scope (one thread of a one-CTA kernel).
+ * moe_ep_wait_signal: a one-thread kernel on `stream` polls *signal (acquire)
+ * until it is >= expected, then subtracts expected; if timeout_ns (1 .. 10^10)
+ * pass first, it latches MOE_EP_DEVERR_TIMEOUT in g's device-error word,
+ * leaves *signal alone and returns, and g's next call returns
+ * MOE_EP_ERR_TIMEOUT.  The producers of the signal must be ordered before the
+ * wait on the GPU (the same stream, or an event the stream waits for): the
+ * wait checks that their signals arrived, it does not stand in for that
+ * ordering -- one GPU never guarantees that a kernel still queued elsewhere
+ * runs while another waits for it.  Errors: MOE_EP_ERR_INVALID for a null or
+ * misaligned signal or a limit outside the range. */
+MOE_EP_API int moe_ep_signal_add(moe_ep_group_t g, uint32_t* signal, uint32_t value,
+                                 moe_ep_stream_t stream);
+MOE_EP_API int moe_ep_wait_signal(moe_ep_group_t g, uint32_t* signal, uint32_t expected,
+                                  int64_t timeout_ns, moe_ep_stream_t stream);
 
 /* Pad every HT expert block of the receive layout to a multiple of `align`
  * rows (a power of two, 1..1024; 1 = dense, the default) for the routes that
@@ -353,7 +385,9 @@ MOE_EP_API int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off,
  * pre-placed buffers.  (The source pages have no counterpart: there every
  * rank allocates its communication buffers at group creation.)
  * Computes what moe_ep_route followed by moe_ep_copy_layout computes on a
- * handle of the same mode, experts, ranks and slots, with the same options:
+ * handle of the same mode, experts, ranks and slots, with the same options
+ * and the default row alignment of 1 (dense HT expert blocks; there is no
+ * alignment argument):
  * topk_idx [T][k], topk_w [T][k] (may be NULL), row [T][k], cnt [E],
  * off [E+1], rcnt [R], roff [R+1], all device buffers owned by the caller.
  * The layout's scratch lives in one static device array of 346.25 KiB that every
@@ -361,9 +395,12 @@ MOE_EP_API int moe_ep_copy_layout(moe_ep_handle_t h, int32_t* cnt, int32_t* off,
  * Capacity: ceil(num_tokens / 32) * experts <= 65536 (e.g. 8192 tokens with
  * 256 experts); larger sizes return MOE_EP_ERR_OVERFLOW without launching.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the array: calls whose work overlaps on the GPU
- * (different streams without ordering) race; calls on one stream do not.
+ * device, with that device current) and keeps it for the life of the
+ * process; make that first call before any stream capture, and do not call
+ * this entry point again after cudaDeviceReset (or any teardown of the
+ * device's primary context): the kept address would be stale.  Every call
+ * shares the array: calls whose work overlaps on the GPU (different streams
+ * without ordering) race; calls on one stream do not.
  * mode: MOE_EP_LL or MOE_EP_HT; slots: S for LL (>= num_tokens), ignored for HT.
  * Asynchronous on `stream`. */
 MOE_EP_API int moe_ep_route_layout_static(const float* scores, int num_tokens, int experts,
