@@ -202,13 +202,264 @@ def whole_job_rate(tokens_per_rank: int, world: int, steps: int, ms: float) -> f
     return tokens_per_rank * world * steps / (ms / 1e3)
 
 
+# ------------------------------------------------------------------ timing
+def agreed_passes(first_pass_ms: float, min_seconds: float, max_passes: int = 2000,
+                  device=None) -> int:
+    """Timed passes of K steps every rank runs: enough for min_seconds of GPU
+    time at the slowest rank's first-pass time, at least 3.  Every rank gets
+    the same number (the barriers around each pass must pair up)."""
+    ms = reduce_max_over_ranks(max(first_pass_ms, 1e-3), device)
+    return int(min(max_passes, max(3, -(-min_seconds * 1e3 // ms))))
+
+
+def numa_of_buffer(addr: int, nbytes: int) -> dict:
+    """NUMA nodes holding the pages of [addr, addr + nbytes): pages per node,
+    from /proc/self/maps and /proc/self/numa_maps (Linux)."""
+    try:
+        spans = []
+        with open("/proc/self/maps") as f:
+            for line in f:
+                a, b = line.split()[0].split("-")
+                spans.append((int(a, 16), int(b, 16)))
+        nodes: dict[str, int] = {}
+        with open("/proc/self/numa_maps") as f:
+            for line, (a, b) in zip(f, spans):
+                if b <= addr or a >= addr + nbytes:
+                    continue
+                for tok in line.split()[1:]:
+                    m = re.fullmatch(r"N(\d+)=(\d+)", tok)
+                    if m:
+                        nodes[m.group(1)] = nodes.get(m.group(1), 0) + int(m.group(2))
+        return nodes
+    except Exception as e:   # not Linux, or the files are not readable
+        return {"unknown": str(e)}
+
+
+def gpu_numa_node(pci_bus_id: str | None) -> int | None:
+    """The NUMA node the GPU's PCI function reports (-1: none)."""
+    if not pci_bus_id:
+        return None
+    bus = pci_bus_id.lower()
+    if bus.count(":") == 2 and len(bus.split(":")[0]) == 8:
+        bus = bus[4:]                                   # 00000000:xx:... -> 0000:xx:...
+    try:
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            return int(f.read().strip())
+    except Exception:
+        return None
+
+
+def measure_link(dev, nbytes: int = 256 << 20, reps: int = 5) -> dict:
+    """Host<->device copy bandwidth with pinned host memory: host->device,
+    device->host and both directions at once (two streams), best of `reps`,
+    CUDA events; and where the pinned pages live."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_in.fill_(1)
+    h_out.fill_(2)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, streams):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0 = [torch.cuda.Event(enable_timing=True) for _ in streams]
+            e1 = [torch.cuda.Event(enable_timing=True) for _ in streams]
+            for s, e in zip(streams, e0):
+                e.record(s)
+            fn()
+            for s, e in zip(streams, e1):
+                e.record(s)
+            torch.cuda.synchronize(dev)
+            t = max(e0[0].elapsed_time(b) for b in e1)
+            best = min(best, t)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in = timed(h2d, [s1])
+    t_out = timed(d2h, [s2])
+    t_both = timed(both, [s1, s2])
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=uuid,pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout
+        uuid = str(props.uuid).replace("GPU-", "")
+        for line in out.splitlines():
+            u, b = [x.strip() for x in line.split(",")]
+            if uuid in u:
+                bus = b
+    except Exception:
+        pass
+    cpus = sorted(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else []
+    return {"h2d_GBps": nbytes / (t_in / 1e3) / 1e9, "d2h_GBps": nbytes / (t_out / 1e3) / 1e9,
+            "both_GBps": 2 * nbytes / (t_both / 1e3) / 1e9, "bytes_per_copy": nbytes,
+            "how": f"pinned host memory (torch pin_memory), copy_ on its own stream, best of {reps}; "
+                   "both = one copy each way at once on two streams",
+            "numa": {"pinned_in_pages_by_node": numa_of_buffer(h_in.data_ptr(), nbytes),
+                     "pinned_out_pages_by_node": numa_of_buffer(h_out.data_ptr(), nbytes),
+                     "gpu_pci": bus, "gpu_numa_node": gpu_numa_node(bus),
+                     "cpus_allowed": f"{cpus[0]}-{cpus[-1]} ({len(cpus)})" if cpus else None}}
+
+
 # ------------------------------------------------------------------ GPU arm
+class WorkloadRun:
+    """One workload on fixed buffers: its pipeline, inputs and bound step."""
+
+    def __init__(self, w: synth.Workload, dev, stream, rank: int, dedup: bool = False):
+        import torch
+
+        from combine_layout_gb300 import moe_ep as ep
+        from combine_layout_gb300.pipeline import BoundStep, EpPipeline
+        self.w, self.dev, self.stream, self.dedup = w, dev, stream, dedup
+        inp = synth.make_inputs(w, seed=w.seed + rank)
+        self.scores_h = torch.from_numpy(inp["scores"]).pin_memory()
+        self.x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.scores = self.scores_h.to(dev)
+        self.x = self.x_h.to(dev)
+        # x is resident (or, end to end, uploaded) before each step's route and
+        # nothing writes it between the route and the dispatch: the MoE-layer
+        # order, so the dispatch may read its tokens while the router finishes
+        self.p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=dev,
+                            x_before_route=True)
+        if w.fp8:
+            g = torch.Generator(device=dev)
+            g.manual_seed(1234 + rank)
+            self.y = torch.randn((self.p.rows, w.H), generator=g, device=dev,
+                                 dtype=torch.float32).to(torch.bfloat16)
+        else:
+            self.y = self.p.recv_x
+        self.ht = w.mode == ep.MOE_EP_HT
+        if dedup and not self.ht:
+            raise SystemExit("--path dedup needs an HT workload")
+        # The HT receive-count query (the mode's one host synchronisation)
+        # comes last: the receive buffers hold the worst case (T*k rows), so
+        # neither the dispatch nor the combine launch waits for the count,
+        # and the sync overlaps the step's GPU work instead of splitting it.
+        self.bs = BoundStep(self.p, self.scores, self.x, self.y, w.T, w.G, w.kg, 0,
+                            w.weight_mode, stream)
+
+    def step(self, ev=None):
+        p, bs, s = self.p, self.bs, self.stream
+        if ev is not None:
+            ev[0].record(s)
+        bs.route()
+        if ev is not None:
+            ev[1].record(s)
+        if self.dedup:
+            p.dispatch_dedup(self.x, s)
+            p.expand(s)
+        else:
+            bs.dispatch()
+        if ev is not None:
+            ev[2].record(s)
+        if self.dedup:
+            p.combine_dedup(self.y, stream=s)
+        else:
+            bs.combine()
+        if ev is not None:
+            ev[3].record(s)
+        if self.ht:
+            bs.num_recv_tokens()
+
+    def timed(self, steps: int, warmup: int, min_seconds: float, barrier, uuid) -> dict:
+        """W warm-up steps; passes of exactly K steps, each bracketed by a
+        barrier and a synchronize and timed with CUDA events on the launching
+        stream, repeated (the same count on every rank) until min_seconds of
+        GPU time; then one more K-step pass with events between the kernels.
+        Clocks are sampled over all of it."""
+        import torch
+        dev, s = self.dev, self.stream
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(uuid)
+        time.sleep(0.1)
+
+        def one_pass():
+            barrier()
+            torch.cuda.synchronize(dev)
+            t0.record(s)
+            for _ in range(steps):
+                self.step()
+            t1.record(s)
+            torch.cuda.synchronize(dev)
+            barrier()
+            return t0.elapsed_time(t1)
+
+        passes = [one_pass()]
+        n = agreed_passes(passes[0], min_seconds, device=dev)
+        passes += [one_pass() for _ in range(n - 1)]
+        # Per-kernel durations for the roofline: one more K-step pass with
+        # events recorded between the kernels.  An event between two kernels
+        # ends the overlap of the second kernel's launch with the first one's
+        # tail (every kernel is launched with programmatic stream
+        # serialization), so these durations are taken in a pass of their own.
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            self.step(evs[i])
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        barrier()
+        return {"pass_ms": passes, "clocks": clk,
+                "r_ms": [e[0].elapsed_time(e[1]) for e in evs],
+                "d_ms": [e[1].elapsed_time(e[2]) for e in evs],
+                "c_ms": [e[2].elapsed_time(e[3]) for e in evs]}
+
+    def close(self):
+        self.p.close()
+
+
+def secondary_line(w: synth.Workload, r: dict, steps: int) -> dict:
+    """Per-workload figures for the `secondary` object: the step time (median
+    pass), each kernel's event-timed duration and its algorithmic bandwidth
+    against the measured copy peak and the nominal 8 TB/s."""
+    ab = algorithmic_bytes(w)
+    peak, _ = measured_peak_gbs()
+    step_ms = statistics.median(r["pass_ms"]) / steps
+    d = statistics.mean(r["d_ms"])
+    c = statistics.mean(r["c_ms"])
+    ro = statistics.mean(r["r_ms"])
+    gbs = lambda b, ms: b / (ms / 1e3) / 1e9  # noqa: E731
+    total = ab["route"] + ab["dispatch"] + ab["combine"]
+    return {"T": w.T, "H": w.H, "E": w.E, "k": w.k,
+            "mode": "HT" if w.mode == synth.MODE_HT else "LL", "fp8": w.fp8,
+            "step_us": step_ms * 1e3, "tokens_per_s": w.T / (step_ms / 1e3),
+            "passes": len(r["pass_ms"]),
+            "route_us": ro * 1e3, "dispatch_us": d * 1e3, "combine_us": c * 1e3,
+            "dispatch_GBps": gbs(ab["dispatch"], d), "combine_GBps": gbs(ab["combine"], c),
+            "dispatch_frac": gbs(ab["dispatch"], d) / peak,
+            "combine_frac": gbs(ab["combine"], c) / peak,
+            "dispatch_frac_of_8TBps": gbs(ab["dispatch"], d) / 8000.0,
+            "combine_frac_of_8TBps": gbs(ab["combine"], c) / 8000.0,
+            "step_GBps": gbs(total, step_ms),
+            "route_layout_query_us_by_difference": (step_ms - d - c) * 1e3,
+            "event_timing": "route, dispatch and combine each between CUDA events (no launch "
+                            "overlap) in one more pass of K steps",
+            "algorithmic_bytes": ab, "clocks": r["clocks"]}
+
+
 def run_gpu(args) -> dict | None:
     import torch
     import torch.distributed as dist
-
-    from combine_layout_gb300 import moe_ep as ep
-    from combine_layout_gb300.pipeline import BoundStep, EpPipeline
 
     world, rank, local = rank_env()
     if world > 1:
@@ -216,56 +467,8 @@ def run_gpu(args) -> dict | None:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-
-    w = synth.WORKLOADS[args.workload]
-    inp = synth.make_inputs(w, seed=w.seed + rank)
-    scores_h = torch.from_numpy(inp["scores"]).pin_memory()
-    x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    scores = scores_h.to(dev)
-    x = x_h.to(dev)
-    # x is resident (or, end to end, uploaded) before each step's route and
-    # nothing writes it between the route and the dispatch: the MoE-layer
-    # order, so the dispatch may read its tokens while the router finishes
-    p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=dev,
-                   x_before_route=True)
-    if w.fp8:
-        g = torch.Generator(device=dev)
-        g.manual_seed(1234 + rank)
-        y = torch.randn((p.rows, w.H), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    else:
-        y = p.recv_x
-    ht = w.mode == ep.MOE_EP_HT
     stream = torch.cuda.current_stream(dev)
-
-    # The HT receive-count query (the mode's one host synchronisation) comes
-    # last: the receive buffers hold the worst case (T*k rows), so neither the
-    # dispatch nor the combine launch waits for the count, and the sync overlaps
-    # the step's GPU work instead of splitting it.
-    bs = BoundStep(p, scores, x, y, w.T, w.G, w.kg, 0, w.weight_mode, stream)
-
-    dedup = args.path == "dedup"
-    if dedup and not ht:
-        raise SystemExit("--path dedup needs an HT workload")
-
-    def step(ev=None):
-        bs.route()
-        if ev is not None:
-            ev[0].record(stream)
-        if dedup:
-            p.dispatch_dedup(x, stream)
-            p.expand(stream)
-        else:
-            bs.dispatch()
-        if ev is not None:
-            ev[1].record(stream)
-        if dedup:
-            p.combine_dedup(y, stream=stream)
-        else:
-            bs.combine()
-        if ev is not None:
-            ev[2].record(stream)
-        if ht:
-            bs.num_recv_tokens()
+    uuid = str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
 
     def barrier():
         if world > 1:
@@ -274,55 +477,32 @@ def run_gpu(args) -> dict | None:
     def max_over_ranks(v: float) -> float:
         return reduce_max_over_ranks(v, dev)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
-    # --- device-resident timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    uuid = str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
-    barrier()
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(uuid)
-    time.sleep(0.05)
-    t0.record(stream)
-    for i in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    ms_local = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms_local)
-    # Per-kernel durations for the roofline: the same K steps again, with
-    # events recorded between the kernels.  An event between two kernels ends
-    # the overlap of the second kernel's launch with the first one's tail
-    # (every kernel is launched with programmatic stream serialization), so
-    # these durations are taken in a pass of their own.
-    barrier()
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        step(evs[i])
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    barrier()
-    d_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    c_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    w = synth.WORKLOADS[args.workload]
+    dedup = args.path == "dedup"
+    run = WorkloadRun(w, dev, stream, rank, dedup)
+    p = run.p
+    r = run.timed(args.steps, args.warmup, args.min_seconds, barrier, uuid)
+    # the job's time: each rank's median pass, the slowest rank's
+    ms = max_over_ranks(statistics.median(r["pass_ms"]))
+    d_ms, c_ms, clk = r["d_ms"], r["c_ms"], r["clocks"]
+    clk["route_us_event_timed"] = statistics.mean(r["r_ms"]) * 1e3
+    clk["passes"] = len(r["pass_ms"])
 
     nd = int(p.rank_off[-1].item()) if dedup else None
     if dedup:                       # the direct path's end-to-end leg only
-        p.close()
+        run.close()
         if world > 1:
             dist.destroy_process_group()
         if rank != 0:
             return None
-        return _line(args, w, world, ms, d_ms, c_ms, clk, p.rows, ht, None, None, nd)
+        return _line(args, w, world, ms, d_ms, c_ms, clk, p.rows, run.ht, None, None, nd)
 
     # --- end to end: every step copies its inputs (scores, tokens) from pinned
     # host memory and its combined output back.  Inputs and outputs are double
     # buffered on the device, so the copies of neighbouring steps run on their
     # own streams while this step's kernels run.
+    from combine_layout_gb300.pipeline import BoundStep
+    scores_h, x_h, scores, x, y, ht = run.scores_h, run.x_h, run.scores, run.x, run.y, run.ht
     out_h = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     sc_d = [scores, torch.empty_like(scores)]
     x_d = [x, torch.empty_like(x)]
@@ -391,17 +571,43 @@ def run_gpu(args) -> dict | None:
     else:
         rt = None
 
-    p.close()
+    run.close()
+    del sc_d, x_d, out_d, steps_b, run, p
+    torch.cuda.empty_cache()
+    link = measure_link(dev) if rank == 0 else None
+
+    # --- the other workloads, same process and GPU, one line's `secondary`
+    secondary = {}
+    if world == 1 and args.secondary:
+        for name in args.secondary.split(","):
+            if name == w.name:
+                continue
+            ws = synth.WORKLOADS[name]
+            rs = WorkloadRun(ws, dev, stream, rank)
+            r2 = rs.timed(args.steps, args.warmup, args.secondary_seconds, barrier, uuid)
+            rs.close()
+            del rs
+            torch.cuda.empty_cache()
+            secondary[name] = secondary_line(ws, r2, args.steps)
+
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return None
+    h2d = scores_h.numel() * 4 + x_h.numel() * 2
+    d2h = out_h[0].numel() * 2
     e2e = {"value": whole_job_rate(w.T, world, e2e_steps, e2e_ms), "unit": UNIT,
-           "h2d_bytes_per_step": scores_h.numel() * 4 + x_h.numel() * 2,
-           "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": e2e_steps,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "overlap": "double-buffered inputs/outputs; copies on their own streams; each "
-                      "step enqueues the next step's upload before its count query"}
-    return _line(args, w, world, ms, d_ms, c_ms, clk, p.rows, ht, e2e, rt, None)
+                      "step enqueues the next step's upload before its count query",
+           "link_GBps": (h2d + d2h) / (e2e_ms / e2e_steps / 1e3) / 1e9}
+    if link is not None:
+        e2e["link_peak"] = link
+        e2e["link_frac_of_both"] = e2e["link_GBps"] / link["both_GBps"]
+    line = _line(args, w, world, ms, d_ms, c_ms, clk, w.recv_rows(), ht, e2e, rt, None)
+    if secondary:
+        line["secondary"] = secondary
+    return line
 
 
 def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
@@ -410,6 +616,7 @@ def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
     ab = algorithmic_bytes(w) if nd is None else algorithmic_bytes_dedup(w, nd)
     d_avg = statistics.mean(d_ms)
     c_avg = statistics.mean(c_ms)
+    route_us = clk.pop("route_us_event_timed", None)
     dom = "dispatch" if d_avg >= c_avg else "combine"
     dom_ms = d_avg if dom == "dispatch" else c_avg
     peak, peak_src = measured_peak_gbs()
@@ -435,9 +642,16 @@ def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": ab[dom]},
+        "timing": {"passes": clk.get("passes"),
+                   "how": "passes of exactly K steps, each bracketed by a barrier and a "
+                          "synchronize and timed with CUDA events on the launching stream, "
+                          "repeated until >= --min-seconds of GPU time; ms_per_step is the "
+                          "median pass / K (max over ranks)",
+                   "sm_kcycles_per_step": (ms / args.steps * clk["sm_mhz"]
+                                           if clk.get("sm_mhz") else None)},
         "breakdown": {
-            "timing": "second pass of the same K steps with CUDA events between the kernels",
-            "dispatch_us": d_avg * 1e3, "combine_us": c_avg * 1e3,
+            "timing": "one more pass of K steps with CUDA events between the kernels",
+            "route_us": route_us, "dispatch_us": d_avg * 1e3, "combine_us": c_avg * 1e3,
             "dispatch_GBps": ab["dispatch"] / (d_avg / 1e3) / 1e9,
             "combine_GBps": ab["combine"] / (c_avg / 1e3) / 1e9,
             "dispatch_frac": ab["dispatch"] / (d_avg / 1e3) / 1e9 / peak,
@@ -510,8 +724,40 @@ def run_reference(args):
             "data": "synthetic (seeded numpy)", "impl": "reference",
             "config": workload_config(w, args.gpus, rows),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "host_cores": os.cpu_count(), "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _oracle_worker(name: str, scores, x, seconds: float):
+    """One process of the all-core CPU baseline: the oracle on its own copy of
+    the token sample, repeated for `seconds`.  Returns (tokens, seconds)."""
+    import oracle as orc
+    w = synth.WORKLOADS[name]
+    T = x.shape[0]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(orc, w, scores, x, T)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return T * n, el
+
+
+def cpu_oracle_rate_all_cores(w: synth.Workload, sample_tokens: int, seconds: float):
+    """The oracle on every host core at once (one spawned process per core,
+    each on the same token sample): tokens of all processes over the longest
+    one's time."""
+    import multiprocessing as mp
+
+    import oracle as orc
+    orc.build()
+    n = os.cpu_count() or 1
+    inp = synth.make_inputs(w)
+    T = min(sample_tokens, w.T)
+    args = [(w.name, inp["scores"][:T].copy(), inp["x"][:T].copy(), seconds)] * n
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.starmap(_oracle_worker, args)
+    return sum(r[0] for r in res) / max(r[1] for r in res), n
 
 
 def main():
@@ -522,7 +768,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ht_prefill", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--cpu-all-core-seconds", type=float, default=4.0)
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="repeat the K-step timed pass until this much GPU time has passed")
+    ap.add_argument("--secondary", default="ht_prefill_fp8,skewed,mixtral,ll_decode",
+                    help="other workloads measured in the same process (N = 1), '' for none")
+    ap.add_argument("--secondary-seconds", type=float, default=0.25)
+    ap.add_argument("--link-peak", action="store_true",
+                    help="only measure the host<->device copy bandwidth and print it")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="direct", choices=["direct", "dedup"],
@@ -537,6 +791,12 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
+    if args.link_peak:
+        import torch
+        link = measure_link(torch.device("cuda", 0))
+        print(json.dumps({"metric": "host<->device copy GB/s (pinned host memory)", **link}),
+              flush=True)
+        return
 
     line = run_gpu(args)
     if line is None:
@@ -545,8 +805,17 @@ def main():
         rate, T, n, el = cpu_oracle_rate(synth.WORKLOADS[args.workload], args.cpu_sample_tokens,
                                          args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "host_cores": os.cpu_count(),
                                 "sample": f"{n} oracle steps of the first {T} tokens "
                                           f"(full H, E, k) in {el:.1f} s, single thread"}
+        if args.cpu_all_core_seconds > 0:
+            rate_all, ncores = cpu_oracle_rate_all_cores(
+                synth.WORKLOADS[args.workload], args.cpu_sample_tokens, args.cpu_all_core_seconds)
+            line["cpu_baseline"]["all_cores"] = {
+                "value": rate_all, "cores": ncores,
+                "sample": f"one process per host core, each repeating the oracle on the first "
+                          f"{min(args.cpu_sample_tokens, synth.WORKLOADS[args.workload].T)} "
+                          f"tokens for {args.cpu_all_core_seconds:.0f} s"}
     else:
         line["cpu_baseline"] = None
     print(json.dumps(line), flush=True)

@@ -37,10 +37,11 @@ constexpr int kSplitMaxTokens = 1024;
 
 __device__ __forceinline__ uint32_t score_key(float x)
 {
-    if (isnan(x)) x = -INFINITY;
-    if (x == 0.f) x = 0.f;  // -0 -> +0
+    // fmaxf returns the other operand for a NaN (so NaN -> -inf); adding +0
+    // turns -0 into +0 (round to nearest) and leaves every other value alone
+    x = __fadd_rn(fmaxf(x, -INFINITY), 0.f);
     const uint32_t u = __float_as_uint(x);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_score(uint32_t k)
@@ -78,12 +79,16 @@ __device__ __forceinline__ void cx(uint32_t& ka, int& ia, uint32_t& kb, int& ib)
     ib = i1;
 }
 
-// Sort a lane's candidates best first.  Eight: the optimal 19-comparator
-// network; other sizes: odd-even transposition (EPL rounds).
+// Sort a lane's candidates best first.  Eight and four: the optimal 19- and
+// 5-comparator networks; other sizes: odd-even transposition (EPL rounds).
 template <int EPL>
 __device__ __forceinline__ void sort_desc(uint32_t (&k)[EPL], int (&ix)[EPL])
 {
-    if constexpr (EPL == 8) {
+    if constexpr (EPL == 4) {
+        constexpr int net[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
+#pragma unroll
+        for (int c = 0; c < 5; ++c) cx(k[net[c][0]], ix[net[c][0]], k[net[c][1]], ix[net[c][1]]);
+    } else if constexpr (EPL == 8) {
         constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
                                     {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
                                     {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
@@ -97,7 +102,41 @@ __device__ __forceinline__ void sort_desc(uint32_t (&k)[EPL], int (&ix)[EPL])
     }
 }
 
-template <int EPL, bool VEC, int MG>
+// k picks from lane-sorted candidate lists: each pick is the largest head key
+// of the warp, then the lowest expert index holding it; the winning lane pops
+// its head.  Lane j keeps pick j; den sums the picked scores in pick order.
+template <int N>
+__device__ __forceinline__ void pick_k(uint32_t (&key)[N], int (&ix)[N], int k, int lane,
+                                       int& my_i, uint32_t& my_k, uint32_t& first_k, float& den)
+{
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+        const uint32_t hk = key[0];
+        const uint32_t mk = __reduce_max_sync(kFull, hk);
+        const uint32_t wi = __reduce_min_sync(kFull, (hk == mk) ? (uint32_t)ix[0] : 0xffffffffu);
+        const bool found = mk != 0u;
+        if (found && hk == mk && (uint32_t)ix[0] == wi) {
+#pragma unroll
+            for (int i = 0; i + 1 < N; ++i) {
+                key[i] = key[i + 1];
+                ix[i] = ix[i + 1];
+            }
+            key[N - 1] = 0u;
+        }
+        if (lane == j) {
+            my_i = found ? (int)wi : -1;  // not found is unreachable while kg * gs >= k
+            my_k = mk;
+        }
+        if (j == 0) first_k = mk;
+        den += key_score(mk);
+    }
+}
+
+// REDIST: the node-limited routing of 256 experts in 8 groups of 32 with 4
+// groups kept (lanes of 8 experts, 4 lanes per group): the kept groups'
+// experts are spread over the whole warp before the picks (4 per lane
+// instead of 8 on half the lanes), which halves the sort and the pops.
+template <int EPL, bool VEC, int MG, bool REDIST>
 __device__ __forceinline__ void route_token(const float* __restrict__ s, const RouteParams& p,
                                             int lane, int& out_idx, float& out_w)
 {
@@ -177,38 +216,46 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
         if (grp >= p.G || rank >= p.kg) rem = 0u;
     }
 
-    // k picks from lane-sorted candidates: the largest head key, then the
-    // lowest expert index holding it; the winning lane pops its head
-    int ix[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        if (!((rem >> i) & 1u)) key[i] = 0u;  // banned or absent: below every score
-        ix[i] = base + i;
-    }
-    sort_desc<EPL>(key, ix);
     int my_i = -1;
     uint32_t my_k = 0u, first_k = 0u;
     float den = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < p.k; ++j) {
-        const uint32_t hk = key[0];
-        const uint32_t mk = __reduce_max_sync(kFull, hk);
-        const uint32_t wi = __reduce_min_sync(kFull, (hk == mk) ? (uint32_t)ix[0] : 0xffffffffu);
-        const bool found = mk != 0u;
-        if (found && hk == mk && (uint32_t)ix[0] == wi) {
+    if constexpr (REDIST) {
+        // 8 groups of 32 experts (4 lanes of 8 each), 4 kept: gather the 128
+        // kept experts onto all 32 lanes, 4 consecutive experts per lane, lanes
+        // in ascending expert order (kept slot q = lane / 8 holds the q-th
+        // kept group by index; lane pair (2l, 2l+1) of the slot takes source
+        // lane l's two halves).  Exactly 4 group leaders are kept.
+        uint32_t kept = __ballot_sync(kFull, sub == 0 && grp < p.G && (rem != 0u));
+        const int q = lane >> 3;
 #pragma unroll
-            for (int i = 0; i + 1 < EPL; ++i) {
-                key[i] = key[i + 1];
-                ix[i] = ix[i + 1];
-            }
-            key[EPL - 1] = 0u;
+        for (int i = 0; i < 3; ++i)
+            if (i < q) kept &= kept - 1u;  // drop the q lowest kept leaders
+        const int sgrp = (__ffs(kept) - 1) >> p.lpg_log2;
+        const int src = (sgrp << p.lpg_log2) + ((lane >> 1) & 3);
+        const bool upper = lane & 1;
+        uint32_t ck[4];
+        int ci[4];
+        const int cbase = sgrp * p.gs + ((lane >> 1) & 3) * 8 + (upper ? 4 : 0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t a = __shfl_sync(kFull, key[r], src);
+            const uint32_t b = __shfl_sync(kFull, key[4 + r], src);
+            ck[r] = upper ? b : a;
+            ci[r] = cbase + r;
         }
-        if (lane == j) {
-            my_i = found ? (int)wi : -1;  // not found is unreachable while kg * gs >= k
-            my_k = mk;
+        sort_desc<4>(ck, ci);
+        pick_k<4>(ck, ci, p.k, lane, my_i, my_k, first_k, den);
+    } else {
+        // k picks from lane-sorted candidates (banned or absent: key 0, below
+        // every score)
+        int ix[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            if (!((rem >> i) & 1u)) key[i] = 0u;
+            ix[i] = base + i;
         }
-        if (j == 0) first_k = mk;
-        den += key_score(mk);
+        sort_desc<EPL>(key, ix);
+        pick_k<EPL>(key, ix, p.k, lane, my_i, my_k, first_k, den);
     }
 
     const bool act = lane < p.k;
@@ -248,7 +295,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
 // share a tile, each writing its own byte of every tile word (the bits of its
 // 8 tokens), so four times as many SMs do the selection work; the last CTA
 // then derives the byte counts from the words.
-template <int EPL, bool VEC, int MG, int TPC>
+template <int EPL, bool VEC, int MG, int TPC, bool REDIST = false>
 __global__ void __launch_bounds__(TPC * 32, TPC == kTileTokens ? 1 : 2) route_kernel(
     const float* __restrict__ scores, int T, RouteParams p, int32_t* __restrict__ topk_idx,
     int32_t* __restrict__ idx_copy, float* __restrict__ topk_w, LayoutArgs la)
@@ -267,7 +314,7 @@ __global__ void __launch_bounds__(TPC * 32, TPC == kTileTokens ? 1 : 2) route_ke
     if (t < T) {
         int e;
         float w;
-        route_token<EPL, VEC, MG>(scores + (size_t)t * p.E, p, lane, e, w);
+        route_token<EPL, VEC, MG, REDIST>(scores + (size_t)t * p.E, p, lane, e, w);
         if (lane < p.k) {
             const size_t q = (size_t)t * p.k + lane;
             topk_idx[q] = e;
@@ -437,6 +484,22 @@ cudaError_t launch_route_mg(const float* scores, int T, const RouteParams& p, in
     const int ntiles = (T + kTileTokens - 1) / kTileTokens;
     // the group list holds MG >= m keys (m = 1, 2: two; 3, 4: four)
     const bool mg2 = !p.limit || p.m <= 2;
+    if constexpr (EPL == 8 && VEC) {
+        // 8 groups of 32 experts, 4 kept (every lane holds a whole group's
+        // quarter): the kept experts are spread over the warp before the picks
+        if (p.limit && p.m <= 2 && p.G == 8 && p.lpg == 4 && p.gs == 32 && p.kg == 4) {
+            if (T <= kSplitMaxTokens) {
+                LayoutArgs lt = tail_planned(la, 256);
+                lt.cnt_from_words = 1;
+                return launch_pdl(route_kernel<8, true, 2, 8, true>,
+                                  dim3(ntiles * (kTileTokens / 8)), dim3(256), s, scores, T, p,
+                                  topk_idx, idx_copy, topk_w, lt);
+            }
+            return launch_pdl(route_kernel<8, true, 2, kTileTokens, true>, dim3(ntiles),
+                              dim3(1024), s, scores, T, p, topk_idx, idx_copy, topk_w,
+                              tail_planned(la, 1024));
+        }
+    }
     if (T <= kSplitMaxTokens) {  // small batch: 8 tokens per CTA
         LayoutArgs lt = tail_planned(la, 256);
         lt.cnt_from_words = 1;

@@ -24,7 +24,9 @@ def _worker(rank, world, port, out):
         w, r, l = bench.rank_env()
         assert (w, r, l) == (world, rank, rank)
         ms = bench.reduce_max_over_ranks(10.0 + rank)   # rank 1 is the slowest
-        out[rank] = (ms, bench.whole_job_rate(4096, world, 100, ms))
+        # every rank must run the same number of timed passes (barriers pair up)
+        n = bench.agreed_passes(2.0 + 3.0 * rank, 0.5)
+        out[rank] = (ms, bench.whole_job_rate(4096, world, 100, ms), n)
     finally:
         dist.destroy_process_group()
 
@@ -36,6 +38,7 @@ def test_max_over_ranks_and_whole_job_rate_gloo():
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
     assert out[0][0] == out[1][0] == 11.0
     assert out[0][1] == pytest.approx(4096 * 2 * 100 / 11e-3)
+    assert out[0][2] == out[1][2] == 100     # 500 ms at the slower rank's 5 ms per pass
 
 
 def test_single_process_defaults(monkeypatch):
@@ -88,3 +91,22 @@ def test_profile_hash_ignores_comments_only():
     c = "int f(int x) { return x + 2; }"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_agreed_passes_single_process():
+    import bench
+    assert bench.agreed_passes(3.4, 0.5) == 148      # ceil(500 / 3.4)
+    assert bench.agreed_passes(400.0, 0.5) == 3      # at least three passes
+    assert bench.agreed_passes(0.0001, 0.5, max_passes=2000) == 2000
+
+
+def test_numa_of_buffer_reads_this_process():
+    import numpy as np
+
+    import bench
+    a = np.ones(1 << 22, np.uint8)                   # 4 MiB, touched
+    nodes = bench.numa_of_buffer(a.ctypes.data, a.nbytes)
+    assert isinstance(nodes, dict)
+    if "unknown" not in nodes:
+        assert sum(nodes.values()) >= 1
+    assert bench.gpu_numa_node(None) is None
