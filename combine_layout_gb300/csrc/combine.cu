@@ -87,7 +87,18 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
     // tail instead of a fixed token stride (measured: 16384 tokens x 7168,
     // step 518.3 -> 510.7 us; 8192 x 4096, 69.6 -> 68.4 us).  A send-only
     // launch with no tokens still runs one CTA, for the signal.
-    const int nsplit = (nvec % 16 == 0 && T > 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    int nsplit = (nvec % 16 == 0 && T > 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    if (nsplit > 1) {
+        // a small batch: slices of at most one pass (kThreads vectors), so no
+        // thread waits for its rows twice, while the CTAs still fit in one
+        // wave of resident CTAs
+        const int units = nvec / 16, resident = sm_count * combine_min_ctas(k <= 8 ? 8 : 32);
+        for (int d = nsplit; d <= units; ++d) {
+            if (units % d != 0 || nvec / d > kThreads) continue;
+            if ((int64_t)T * d <= resident) nsplit = d;
+            break;
+        }
+    }
     const int items = T * nsplit;
     const int cap = sm_count * 16;
     int blocks = (nvec / nsplit >= 256 && items >= 2 * cap) ? items : (items < cap ? items : cap);
