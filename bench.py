@@ -574,7 +574,7 @@ def run_gpu(args) -> dict | None:
     run.close()
     del sc_d, x_d, out_d, steps_b, run, p
     torch.cuda.empty_cache()
-    link = measure_link(dev) if rank == 0 else None
+    link = measure_link(dev) if world == 1 else None   # one process: nothing else on the link
 
     # --- the other workloads, same process and GPU, one line's `secondary`
     secondary = {}
