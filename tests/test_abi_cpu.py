@@ -69,6 +69,17 @@ def test_host_argument_checks_without_gpu(lib):
         g = getattr(lib, name)
         g.argtypes = [ctypes.c_void_p, ctypes.c_int]
         assert g(None, 1) == INVALID
+    # the signal primitives and the staged calls reject a null group / handle
+    # on the host, before any CUDA call
+    sa = lib.moe_ep_signal_add
+    sa.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]
+    assert sa(None, None, 1, None) == INVALID
+    ws = lib.moe_ep_wait_signal
+    ws.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int64, ctypes.c_void_p]
+    assert ws(None, None, 1, 1000, None) == INVALID
+    cp = lib.moe_ep_complete
+    cp.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert cp(None, None) == INVALID
     s = lib.moe_ep_status_string
     s.restype = ctypes.c_char_p
     assert s(0) == b"ok" and s(2).startswith(b"more tokens")
