@@ -12,7 +12,9 @@ in HBM; `e2e` adds, every step, the host->device copy of the step's inputs
 output.  `roofline` is for the dominant kernel, from CUDA events recorded
 around its launches on the launching stream, in a second pass of the same K
 timed steps (events between kernels end the overlap of a launch with the
-previous kernel's tail, so the `value` pass carries none).
+previous kernel's tail, so the `value` pass carries none).  Each workload's
+entry also carries its kernels launched back to back (launches overlapping,
+as in a step) and, for LL workloads, the step replayed from a CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ht_prefill]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -424,8 +426,66 @@ class WorkloadRun:
                 "d_ms": [e[1].elapsed_time(e[2]) for e in evs],
                 "c_ms": [e[2].elapsed_time(e[3]) for e in evs]}
 
+    def back_to_back(self, reps: int = 3) -> dict:
+        """Each kernel launched n times in a row between two CUDA events on the
+        launching stream, median of reps: microseconds per launch.  Launches
+        overlap the previous launch's tail, as the kernels of a step do, so
+        these durations carry no event gap (the event-timed ones do)."""
+        import torch
+        n = 200 if self.w.T <= 1024 else 50
+        out = {"launches": n, "how": "n launches of one kernel back to back between two CUDA "
+                                     "events on the launching stream, per launch, median of "
+                                     f"{reps}"}
+        for name, fn in (("route_us", self.bs.route), ("dispatch_us", self.bs.dispatch),
+                         ("combine_us", self.bs.combine)):
+            t = []
+            for _ in range(reps):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(self.dev)
+                a.record(self.stream)
+                for _ in range(n):
+                    fn()
+                b.record(self.stream)
+                torch.cuda.synchronize(self.dev)
+                t.append(a.elapsed_time(b) * 1e3 / n)
+            out[name] = statistics.median(t)
+        return out
+
     def close(self):
         self.p.close()
+
+
+def graph_step_us(w: synth.Workload, dev, rank: int, n: int = 20, reps: int = 5) -> float:
+    """An LL workload's step (route, dispatch, combine: no host synchronisation)
+    captured n times in one CUDA graph on a side stream and replayed: the
+    microseconds per step without host launches (how a decode loop runs it)."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        r = WorkloadRun(w, dev, s, rank)
+        for _ in range(3):
+            r.step()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                r.step()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        t = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(10):
+                g.replay()
+            b.record(s)
+            torch.cuda.synchronize(dev)
+            t.append(a.elapsed_time(b) * 1e3 / (10 * n))
+        del g
+        r.close()
+    return statistics.median(t)
 
 
 def secondary_line(w: synth.Workload, r: dict, steps: int) -> dict:
@@ -454,7 +514,7 @@ def secondary_line(w: synth.Workload, r: dict, steps: int) -> dict:
             "route_layout_query_us_by_difference": (step_ms - d - c) * 1e3,
             "event_timing": "route, dispatch and combine each between CUDA events (no launch "
                             "overlap) in one more pass of K steps",
-            "algorithmic_bytes": ab, "clocks": r["clocks"]}
+            "algorithmic_bytes": ab, "back_to_back": r.get("b2b"), "clocks": r["clocks"]}
 
 
 def run_gpu(args) -> dict | None:
@@ -482,6 +542,7 @@ def run_gpu(args) -> dict | None:
     run = WorkloadRun(w, dev, stream, rank, dedup)
     p = run.p
     r = run.timed(args.steps, args.warmup, args.min_seconds, barrier, uuid)
+    b2b = None if dedup else run.back_to_back()
     # the job's time: each rank's median pass, the slowest rank's
     ms = max_over_ranks(statistics.median(r["pass_ms"]))
     d_ms, c_ms, clk = r["d_ms"], r["c_ms"], r["clocks"]
@@ -585,10 +646,14 @@ def run_gpu(args) -> dict | None:
             ws = synth.WORKLOADS[name]
             rs = WorkloadRun(ws, dev, stream, rank)
             r2 = rs.timed(args.steps, args.warmup, args.secondary_seconds, barrier, uuid)
+            r2["b2b"] = rs.back_to_back()
             rs.close()
             del rs
             torch.cuda.empty_cache()
             secondary[name] = secondary_line(ws, r2, args.steps)
+            if ws.mode == synth.MODE_LL:
+                secondary[name]["step_graph_us"] = graph_step_us(ws, dev, rank)
+                torch.cuda.empty_cache()
 
     if world > 1:
         dist.destroy_process_group()
@@ -605,6 +670,7 @@ def run_gpu(args) -> dict | None:
         e2e["link_peak"] = link
         e2e["link_frac_of_both"] = e2e["link_GBps"] / link["both_GBps"]
     line = _line(args, w, world, ms, d_ms, c_ms, clk, w.recv_rows(), ht, e2e, rt, None)
+    line["breakdown"]["back_to_back"] = b2b
     if secondary:
         line["secondary"] = secondary
     return line
