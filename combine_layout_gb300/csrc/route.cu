@@ -133,13 +133,29 @@ __device__ __forceinline__ void pick_k(uint32_t (&key)[N], int (&ix)[N], int k, 
 }
 
 // REDIST: the node-limited routing of 256 experts in 8 groups of 32 with 4
-// groups kept (lanes of 8 experts, 4 lanes per group): the kept groups'
-// experts are spread over the whole warp before the picks (4 per lane
-// instead of 8 on half the lanes), which halves the sort and the pops.
+// groups kept and the top 8 taken by the sum of each group's best 2 (lanes
+// of 8 experts, 4 lanes per group): the kept groups' experts are spread over
+// the whole warp before the picks (4 per lane instead of 8 on half the
+// lanes), which halves the sort and the pops.
 template <int EPL, bool VEC, int MG, bool REDIST>
-__device__ __forceinline__ void route_token(const float* __restrict__ s, const RouteParams& p,
+__device__ __forceinline__ void route_token(const float* __restrict__ s, const RouteParams& pin,
                                             int lane, int& out_idx, float& out_w)
 {
+    RouteParams p = pin;
+    if constexpr (REDIST) {
+        // the one shape this path serves (checked at launch), as constants:
+        // loop bounds, shifts and lane predicates fold away
+        p.E = 256;
+        p.G = 8;
+        p.gs = 32;
+        p.lpg = 4;
+        p.lpg_log2 = 2;
+        p.epl = 8;
+        p.kg = 4;
+        p.m = 2;
+        p.k = 8;
+        p.limit = 1;
+    }
     const int grp = lane >> p.lpg_log2;
     const int sub = lane & (p.lpg - 1);
     const int first = sub * p.epl;        // offset of my first expert inside the group
@@ -207,11 +223,23 @@ __device__ __forceinline__ void route_token(const float* __restrict__ s, const R
                 if (q < p.m) gsum += (double)key_score(top[q]);
             gk = sum_key(gsum);
         }
+        // ranked by the high word unless two groups share it (then exactly)
+        const uint32_t gh = (uint32_t)(gk >> 32);
         int rank = 0;
+        bool tie = false;
 #pragma unroll 8
         for (int n = 0; n < p.G; ++n) {
-            const unsigned long long o = __shfl_sync(kFull, gk, n << p.lpg_log2);
-            rank += (o > gk || (o == gk && n < grp)) ? 1 : 0;
+            const uint32_t o = __shfl_sync(kFull, gh, n << p.lpg_log2);
+            rank += (o > gh) ? 1 : 0;
+            tie |= (o == gh && n != grp);
+        }
+        if (__any_sync(kFull, tie)) {
+            rank = 0;
+#pragma unroll 8
+            for (int n = 0; n < p.G; ++n) {
+                const unsigned long long o = __shfl_sync(kFull, gk, n << p.lpg_log2);
+                rank += (o > gk || (o == gk && n < grp)) ? 1 : 0;
+            }
         }
         if (grp >= p.G || rank >= p.kg) rem = 0u;
     }
@@ -487,7 +515,8 @@ cudaError_t launch_route_mg(const float* scores, int T, const RouteParams& p, in
     if constexpr (EPL == 8 && VEC) {
         // 8 groups of 32 experts, 4 kept (every lane holds a whole group's
         // quarter): the kept experts are spread over the warp before the picks
-        if (p.limit && p.m <= 2 && p.G == 8 && p.lpg == 4 && p.gs == 32 && p.kg == 4) {
+        if (p.limit && p.m == 2 && p.k == 8 && p.G == 8 && p.lpg == 4 && p.gs == 32 &&
+            p.kg == 4) {
             if (T <= kSplitMaxTokens) {
                 LayoutArgs lt = tail_planned(la, 256);
                 lt.cnt_from_words = 1;
