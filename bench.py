@@ -542,7 +542,7 @@ def run_gpu(args) -> dict | None:
     run = WorkloadRun(w, dev, stream, rank, dedup)
     p = run.p
     r = run.timed(args.steps, args.warmup, args.min_seconds, barrier, uuid)
-    b2b = None if dedup else run.back_to_back()
+    b2b = None if dedup or args.no_b2b else run.back_to_back()
     # the job's time: each rank's median pass, the slowest rank's
     ms = max_over_ranks(statistics.median(r["pass_ms"]))
     d_ms, c_ms, clk = r["d_ms"], r["c_ms"], r["clocks"]
@@ -636,6 +636,8 @@ def run_gpu(args) -> dict | None:
     del sc_d, x_d, out_d, steps_b, run, p
     torch.cuda.empty_cache()
     link = measure_link(dev) if world == 1 else None   # one process: nothing else on the link
+    graph_us = (graph_step_us(w, dev, rank)
+                if w.mode == synth.MODE_LL and not args.no_b2b and world == 1 else None)
 
     # --- the other workloads, same process and GPU, one line's `secondary`
     secondary = {}
@@ -646,12 +648,12 @@ def run_gpu(args) -> dict | None:
             ws = synth.WORKLOADS[name]
             rs = WorkloadRun(ws, dev, stream, rank)
             r2 = rs.timed(args.steps, args.warmup, args.secondary_seconds, barrier, uuid)
-            r2["b2b"] = rs.back_to_back()
+            r2["b2b"] = None if args.no_b2b else rs.back_to_back()
             rs.close()
             del rs
             torch.cuda.empty_cache()
             secondary[name] = secondary_line(ws, r2, args.steps)
-            if ws.mode == synth.MODE_LL:
+            if ws.mode == synth.MODE_LL and not args.no_b2b:
                 secondary[name]["step_graph_us"] = graph_step_us(ws, dev, rank)
                 torch.cuda.empty_cache()
 
@@ -671,6 +673,8 @@ def run_gpu(args) -> dict | None:
         e2e["link_frac_of_both"] = e2e["link_GBps"] / link["both_GBps"]
     line = _line(args, w, world, ms, d_ms, c_ms, clk, w.recv_rows(), ht, e2e, rt, None)
     line["breakdown"]["back_to_back"] = b2b
+    if graph_us is not None:
+        line["breakdown"]["step_graph_us"] = graph_us
     if secondary:
         line["secondary"] = secondary
     return line
@@ -845,6 +849,9 @@ def main():
                     help="only measure the host<->device copy bandwidth and print it")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-b2b", action="store_true",
+                    help="skip the back-to-back kernel and CUDA-graph step timings "
+                         "(profiling runs: fewer launches)")
     ap.add_argument("--path", default="direct", choices=["direct", "dedup"],
                     help="dedup: one copy per (token, rank), expanded on the receiver, "
                          "two-stage combine (HT workloads)")
