@@ -34,16 +34,17 @@ constexpr int combine_min_ctas(int kmax)
 
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kernel(
-    const uint4* __restrict__ y, int T, int k, int nvec, int nsplit,
+    const uint4* __restrict__ y, int T, int k, int nvec, TokenSplit split,
     const int32_t* __restrict__ row, const float* __restrict__ w, uint4* __restrict__ out,
     SendSignal sig)
 {
     griddep_wait();
     __shared__ int s_row[KMAX];
     __shared__ float s_w[KMAX];
-    const int chunk = nvec / nsplit;  // token t's slice sl: vectors [sl*chunk, (sl+1)*chunk)
-    for (int it = blockIdx.x; it < T * nsplit; it += gridDim.x) {
-        const int t = it / nsplit, sl = it - t * nsplit;
+    const int items = split_items(split, T);
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        int t, vb, ve;  // token t's vectors [vb, ve)
+        split_item(split, it, nvec, t, vb, ve);
         if (threadIdx.x < k) {
             s_row[threadIdx.x] = row[(size_t)t * k + threadIdx.x];
             s_w[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
             r[j] = j < k ? s_row[j] : -1;
             wj[j] = j < k ? s_w[j] : 0.f;
         }
-        for (int v = sl * chunk + threadIdx.x; v < (sl + 1) * chunk; v += kThreads) {
+        for (int v = vb + threadIdx.x; v < ve; v += kThreads) {
             uint4 val[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
@@ -83,11 +84,18 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
     // one CTA per token (or per token slice in small batches), at most 16
     // per SM, grid-stride beyond (small tokens then amortise the CTA launch)
     // -- except for rows of 256 vectors or more when there are at least twice
-    // that many tokens: then one CTA per token, so the hardware balances the
-    // tail instead of a fixed token stride (measured: 16384 tokens x 7168,
-    // step 518.3 -> 510.7 us; 8192 x 4096, 69.6 -> 68.4 us).  A send-only
-    // launch with no tokens still runs one CTA, for the signal.
-    int nsplit = (nvec % 16 == 0 && T > 0) ? slices_for(T, nvec / 16, sm_count) : 1;
+    // that many tokens or a sliced tail: then one CTA per item, so the
+    // hardware balances the tail instead of a fixed token stride (measured:
+    // 16384 tokens x 7168, step 518.3 -> 510.7 us; 8192 x 4096, 69.6 -> 68.4
+    // us; 4096 x 7168 with its last 456 tokens in 7 slices, combine 76.4 ->
+    // 74.2 us).  A send-only launch with no tokens still runs one CTA, for
+    // the signal.
+    // tail slices of at most 128 vectors (one pass per thread), from 4 tokens
+    // per SM
+    TokenSplit split = (nvec % 16 == 0 && T > 0)
+                           ? token_split(T, nvec / 16, sm_count, 8, 4 * sm_count)
+                           : TokenSplit{T, 1, 1};
+    int nsplit = split.nsa;
     if (nsplit > 1) {
         // a small batch: slices of at most one pass (kThreads vectors), so no
         // thread waits for its rows twice, while the CTAs still fit in one
@@ -98,16 +106,19 @@ cudaError_t launch_combine(const void* y, int T, int H, int k, const int32_t* ro
             if ((int64_t)T * d <= resident) nsplit = d;
             break;
         }
+        split = TokenSplit{T, nsplit, 1};
     }
-    const int items = T * nsplit;
+    const int items = split_items(split, T);
     const int cap = sm_count * 16;
-    int blocks = (nvec / nsplit >= 256 && items >= 2 * cap) ? items : (items < cap ? items : cap);
+    const bool tail = split.th < T;  // sliced tail: one CTA per item
+    int blocks = (nvec / nsplit >= 256 && (tail || items >= 2 * cap)) ? items
+                                                                      : (items < cap ? items : cap);
     if (blocks < 1) blocks = 1;
     const uint4* yy = (const uint4*)y;
     uint4* oo = (uint4*)out;
 #define MOEEP_COMBINE(KM)                                                                      \
     return launch_pdl(combine_kernel<KM>, dim3(blocks), dim3(kThreads), s, yy, T, k, nvec,     \
-                      nsplit, row, w, oo, sig)
+                      split, row, w, oo, sig)
     if (k <= 1) MOEEP_COMBINE(1);
     if (k <= 2) MOEEP_COMBINE(2);
     if (k <= 4) MOEEP_COMBINE(4);

@@ -215,6 +215,51 @@ cudaError_t launch_finish_words(const LayoutArgs& la, cudaStream_t s);
 // 1 when the tokens alone do.
 int slices_for(int T, int units, int sm_count);
 
+// Work items of a token-parallel kernel (one CTA per item): tokens [0, th)
+// in nsa equal column slices each, tokens [th, T) in nsb.  Small batches:
+// th = T and nsa = slices_for (enough items to fill the GPU).  Large
+// batches: nsa = 1 and the last few hundred tokens in nsb short slices, so
+// the launch's last wave is made of short items and the SMs run out of work
+// at nearly the same time (one CTA per whole token leaves SMs idle for up to
+// a token's duration at the end).  Rows are split in units of 16 vectors.
+struct TokenSplit {
+    int th;
+    int nsa;
+    int nsb;
+};
+
+__host__ __device__ inline int split_items(const TokenSplit& s, int T)
+{
+    return s.th * s.nsa + (T - s.th) * s.nsb;
+}
+
+// The split for T tokens of `units` 16-vector units each, the tail's slices
+// at most max_slice_units long; no sliced tail below min_tokens tokens.
+TokenSplit token_split(int T, int units, int sm_count, int max_slice_units, int min_tokens);
+
+#ifdef __CUDACC__
+// Token and vector range [vb, ve) of work item b (nvec vectors per row).
+__device__ __forceinline__ void split_item(const TokenSplit& s, int b, int nvec, int& t, int& vb,
+                                           int& ve)
+{
+    int sl, ns;
+    if (b < s.th * s.nsa) {
+        ns = s.nsa;
+        t = b / ns;
+        sl = b - t * ns;
+    } else {
+        ns = s.nsb;
+        const int q = b - s.th * s.nsa;
+        const int u = q / ns;
+        sl = q - u * ns;
+        t = s.th + u;
+    }
+    const int ch = nvec / ns;
+    vb = sl * ch;
+    ve = vb + ch;
+}
+#endif
+
 // Dispatch pack: x bf16 [T][H] -> receive rows (bf16 copy or FP8 + scales).
 // Also writes the row map and recv_src, and copies cnt into recv_cnt -- or,
 // with fin != nullptr (a deferred layout), its first CTA finishes the
