@@ -252,3 +252,27 @@ def test_fp8_scale_for_every_bf16_block_maximum():
     pos = rng.integers(0, 128, T * nblk)
     xb[np.arange(T * nblk), pos] = amax                   # the maximum itself
     _fp8_bytes_match_oracle(xb.reshape(T, H).astype(np.uint16))
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("name,per_sm,extra,H", [
+    ("ht_prefill", 4, -1, None), ("ht_prefill", 4, 0, None), ("ht_prefill", 16, -1, None),
+    ("ht_prefill", 16, 0, None), ("ht_prefill", 16, 37, None), ("mixtral", 16, 5, None),
+    ("ht_prefill", 16, 3, 7296)])
+def test_parity_around_the_sliced_tail(name, per_sm, extra, H):
+    """Large batches put their last tokens in column slices (the bf16
+    dispatch from 16 tokens per SM, the combine from 4): token counts on both
+    sides of each threshold, a row width whose 16-vector units split only
+    into odd slices (H = 7296: 57 units), and the 4096-wide rows that take
+    the 64-thread dispatch CTAs -- every element against the oracle."""
+    base = synth.WORKLOADS[name]
+    w = base.with_tokens(per_sm * _sms() + extra)
+    if H is not None:
+        d = dict(w.__dict__)
+        d.pop("extra")
+        d["H"] = H
+        w = synth.Workload(**d)
+    _run(w, x_early=True)
