@@ -82,3 +82,31 @@ def test_parity_sweep(w):
 @pytest.mark.parametrize("w", DEDUP_CASES, ids=_ids(DEDUP_CASES))
 def test_dedup_parity_sweep(w):
     _run_dedup(w)
+
+
+def _large_cases(n: int = 6, seed: int = 4242):
+    """HT batches of 2 500 - 6 000 tokens with rows of 2 048 - 7 168 elements:
+    the regime where the bf16 dispatch and the combine slice their last tokens
+    (unit counts 16 - 56, so the tail slices come in 2 to 7 per row)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for c in _cases(4 * n, seed=seed):
+        if len(out) == n:
+            break
+        if c.mode != synth.MODE_HT:
+            continue
+        d = dict(c.__dict__)
+        d.pop("extra")
+        d["name"] = f"large{len(out)}"
+        d["T"] = int(rng.integers(2500, 6001))
+        d["H"] = int(rng.choice([2048, 3072, 5120, 6144, 7168]))
+        out.append(synth.Workload(**d))
+    return out
+
+
+LARGE_CASES = _large_cases()
+
+
+@pytest.mark.parametrize("w", LARGE_CASES, ids=_ids(LARGE_CASES))
+def test_parity_sweep_large_batches(w):
+    _run(w)
