@@ -46,8 +46,16 @@ def _check_route_layout(w, p, inp):
 
 
 def _run(w, seed=None, x_early=False):
-    inp = synth.make_inputs(w, seed)
     p = _pipeline(w, x_early)
+    d = _check_pass(p, w, synth.make_inputs(w, seed))
+    p.close()
+    return d
+
+
+def _check_pass(p, w, inp):
+    """One forward of w.T tokens on pipeline p (whose group may hold more),
+    every output element against the oracle; returns the combine's ulp
+    differences."""
     scores = torch.from_numpy(inp["scores"]).to(DEV)
     x = to_dev_bf16(inp["x"], DEV)
     p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode)
@@ -93,7 +101,6 @@ def _run(w, seed=None, x_early=False):
     if not w.fp8:
         rt = bf16_ulp_diff(got, inp["x"])
         assert rt.max() <= 1, f"round trip off by {rt.max()} ulp"
-    p.close()
     return d
 
 
@@ -276,3 +283,20 @@ def test_parity_around_the_sliced_tail(name, per_sm, extra, H):
         d["H"] = H
         w = synth.Workload(**d)
     _run(w, x_early=True)
+
+
+@pytest.mark.parametrize("name,max_tokens,sizes", [
+    ("ht_prefill", 4096, (4096, 1, 3000, 257, 2500, 33, 4096)),
+    ("ht_prefill_fp8", 3000, (3000, 77, 2600, 5)),
+    ("ll_decode", 300, (300, 100, 1, 300, 256, 257))])
+def test_one_handle_through_batches_of_changing_size(name, max_tokens, sizes):
+    """One group and handle, forwards of changing size in a row (small and
+    large batches, LL layouts deferred to the dispatch and finished by the
+    router's last CTA, sliced and unsliced tails): the workspace left by one
+    forward must not leak into the next.  Every forward against the oracle."""
+    base = synth.WORKLOADS[name]
+    p = _pipeline(base.with_tokens(max_tokens, slots=max_tokens if base.slots else None))
+    for i, T in enumerate(sizes):
+        w = base.with_tokens(T, slots=max_tokens if base.slots else None)
+        _check_pass(p, w, synth.make_inputs(w, 1000 + i))
+    p.close()
