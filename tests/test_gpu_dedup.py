@@ -37,9 +37,16 @@ def _ulp(bits):
 def _run(w, x_early=False):
     """The whole dedup path against the oracle, every element compared."""
     from combine_layout_gb300.pipeline import EpPipeline
-    inp = synth.make_inputs(w)
     p = EpPipeline(w.mode, w.E, w.R, w.max_tokens, w.H, w.k, fp8=w.fp8, device=DEV,
                    x_before_route=x_early)
+    r = _check_pass(p, w, synth.make_inputs(w))
+    p.close()
+    return r
+
+
+def _check_pass(p, w, inp):
+    """One dedup forward of w.T tokens on pipeline p (whose group may hold
+    more tokens), every element against the oracle."""
     x_d = to_dev_bf16(inp["x"], DEV)
     p.route(torch.from_numpy(inp["scores"]).to(DEV), w.T, w.G, w.kg, 0, w.weight_mode)
     p.dispatch_dedup(x_d)
@@ -106,7 +113,6 @@ def _run(w, x_early=False):
         agree[has] &= dp[qs[has, j]].max(1) == 0
     assert np.all(np.abs(g - o) <= bound * (1 + 1e-6)), "out outside the two-rounding bound"
     assert bf16_ulp_diff(got[agree], want[agree]).max(initial=0) <= 1
-    p.close()
     return nd, nrows
 
 
@@ -234,4 +240,20 @@ def test_dedup_empty_batch():
     p.combine_dedup(p.recv_x)
     torch.cuda.synchronize()
     assert p.rank_cnt.cpu().tolist() == [0] * 4 and p.rank_off.cpu().tolist() == [0] * 5
+    p.close()
+
+
+@pytest.mark.parametrize("name", ["ht_prefill", "ht_prefill_fp8"])
+def test_dedup_through_batches_of_changing_size(name):
+    """One group and handle, dedup forwards of changing size in a row: the
+    rank layout and the dedup row map of one forward must not leak into the
+    next.  Every forward against the oracle."""
+    from combine_layout_gb300.pipeline import EpPipeline
+    base = synth.WORKLOADS[name]
+    big = base.with_tokens(3000)
+    p = EpPipeline(big.mode, big.E, big.R, big.max_tokens, big.H, big.k, fp8=big.fp8,
+                   device=DEV)
+    for i, T in enumerate((3000, 40, 2500, 1, 700)):
+        w = base.with_tokens(T)
+        _check_pass(p, w, synth.make_inputs(w, 2000 + i))
     p.close()
