@@ -15,7 +15,15 @@
 // 16-byte slice before accumulating.  The rows are read with the streaming
 // (evict-first) policy: each is read once, and the bench step measured
 // 179.5 -> 171.2 us with it (the lines the dispatch left dirty in L2 are
-// then not pushed out by rows that are never read again).
+// then not pushed out by rows that are never read again).  Tokens are taken
+// from the last to the first: when the rows were written token by token just
+// before (the dispatch's own output, read back by identity experts, or any
+// token-major producer), the last tokens' rows are the ones still in L2, and
+// they are read before the stream of other rows evicts them (4096 x 7168,
+// k = 8: the dispatch + combine step 164.6 -> 157.0 us; 8192 x 4096, k = 2:
+// 68.0 -> 64.4 us).  Rows written expert by expert (an expert GEMM) have no
+// such order, and the walk then makes no difference (the FP8 workload's
+// separate expert-output buffer: 137.3 us either way).
 #include "bf16x8.cuh"
 #include "common.cuh"
 
@@ -45,6 +53,7 @@ __global__ void __launch_bounds__(kThreads, combine_min_ctas(KMAX)) combine_kern
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         int t, vb, ve;  // token t's vectors [vb, ve)
         split_item(split, it, nvec, t, vb, ve);
+        t = T - 1 - t;  // last token first (see above)
         if (threadIdx.x < k) {
             s_row[threadIdx.x] = row[(size_t)t * k + threadIdx.x];
             s_w[threadIdx.x] = w ? w[(size_t)t * k + threadIdx.x] : 1.f;
