@@ -88,14 +88,35 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+L2_BYTES_NOMINAL = 126 * 2**20  # GB300 (the device's own figure is used when known)
+
+
+def step_bytes(w: synth.Workload) -> int:
+    """Bytes one step touches (route, dispatch and combine: the algorithmic bytes)."""
+    ab = algorithmic_bytes(w)
+    return ab["route"] + ab["dispatch"] + ab["combine"]
+
+
+def flushes_l2(w: synth.Workload, l2_bytes: int = L2_BYTES_NOMINAL) -> bool:
+    """A step that touches less than twice the L2 would find its inputs there
+    from the step before: such workloads flush the L2 before every timed step."""
+    return step_bytes(w) < 2 * l2_bytes
+
+
 def workload_config(w: synth.Workload, world: int, rows: int) -> dict:
     """The `config` of both arms' JSON lines (rows: receive-buffer rows)."""
+    if flushes_l2(w):
+        l2 = (f"step touches {step_bytes(w) / 1e6:.0f} MB, less than twice L2: L2 flushed "
+              "(a read of a buffer twice its size) before every timed step, each step timed "
+              "between its own events")
+    else:
+        l2 = ("inputs larger than L2: each step writes and reads a "
+              f"{rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer "
+              f"({step_bytes(w) / 1e6:.0f} MB touched per step)")
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "ranks": w.R, "k": w.k,
             "nodes": w.G, "max_nodes": w.kg,
             "mode": "HT" if w.mode == synth.MODE_HT else "LL", "fp8": w.fp8,
-            "l2": "inputs larger than L2: each step writes and reads a "
-                  f"{rows * w.H * (1 if w.fp8 else 2) / 1e6:.0f} MB receive buffer",
-            "parallelism": f"replicas x{world} (logical ranks inside each GPU)"}
+            "l2": l2, "parallelism": f"replicas x{world} (logical ranks inside each GPU)"}
 
 
 def _code_only(text: str) -> str:
@@ -354,6 +375,15 @@ class WorkloadRun:
         # and the sync overlaps the step's GPU work instead of splitting it.
         self.bs = BoundStep(self.p, self.scores, self.x, self.y, w.T, w.G, w.kg, 0,
                             w.weight_mode, stream)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES_NOMINAL
+        self.flush = (torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+                      if flushes_l2(w, l2) else None)
+
+    def flush_l2(self):
+        """Read a buffer twice the L2's size on the launching stream: the L2
+        then holds none of the step's data, and only clean lines to evict."""
+        if self.flush is not None:
+            self.flush.max()
 
     def step(self, ev=None):
         p, bs, s = self.p, self.bs, self.stream
@@ -394,7 +424,39 @@ class WorkloadRun:
         clocks = ClockSampler(uuid)
         time.sleep(0.1)
 
+        ea = eb = None
+        if self.flush is not None:
+            ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+
         def one_pass():
+            barrier()
+            torch.cuda.synchronize(dev)
+            if self.flush is None:
+                t0.record(s)
+                for _ in range(steps):
+                    self.step()
+                t1.record(s)
+                torch.cuda.synchronize(dev)
+                barrier()
+                return t0.elapsed_time(t1)
+            # a small step: the L2 is flushed before each step, outside its events
+            for i in range(steps):
+                self.flush_l2()
+                ea[i].record(s)
+                self.step()
+                eb[i].record(s)
+            torch.cuda.synchronize(dev)
+            barrier()
+            return sum(ea[i].elapsed_time(eb[i]) for i in range(steps))
+
+        passes = [one_pass()]
+        n = agreed_passes(passes[0], min_seconds, device=dev)
+        passes += [one_pass() for _ in range(n - 1)]
+        warm = None
+        if self.flush is not None:
+            # context only: the same K steps back to back with no flush (the
+            # step's data stays in L2 from one step to the next)
             barrier()
             torch.cuda.synchronize(dev)
             t0.record(s)
@@ -403,11 +465,7 @@ class WorkloadRun:
             t1.record(s)
             torch.cuda.synchronize(dev)
             barrier()
-            return t0.elapsed_time(t1)
-
-        passes = [one_pass()]
-        n = agreed_passes(passes[0], min_seconds, device=dev)
-        passes += [one_pass() for _ in range(n - 1)]
+            warm = t0.elapsed_time(t1)
         # Per-kernel durations for the roofline: one more K-step pass with
         # events recorded between the kernels.  An event between two kernels
         # ends the overlap of the second kernel's launch with the first one's
@@ -417,11 +475,12 @@ class WorkloadRun:
         barrier()
         torch.cuda.synchronize(dev)
         for i in range(steps):
+            self.flush_l2()
             self.step(evs[i])
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
         barrier()
-        return {"pass_ms": passes, "clocks": clk,
+        return {"pass_ms": passes, "clocks": clk, "warm_pass_ms": warm,
                 "r_ms": [e[0].elapsed_time(e[1]) for e in evs],
                 "d_ms": [e[1].elapsed_time(e[2]) for e in evs],
                 "c_ms": [e[2].elapsed_time(e[3]) for e in evs]}
@@ -435,7 +494,9 @@ class WorkloadRun:
         n = 200 if self.w.T <= 1024 else 50
         out = {"launches": n, "how": "n launches of one kernel back to back between two CUDA "
                                      "events on the launching stream, per launch, median of "
-                                     f"{reps}"}
+                                     f"{reps}" + ("; the same inputs each launch, so a step "
+                                                  "smaller than L2 runs from L2 here"
+                                                  if self.flush is not None else "")}
         for name, fn in (("route_us", self.bs.route), ("dispatch_us", self.bs.dispatch),
                          ("combine_us", self.bs.combine)):
             t = []
@@ -456,12 +517,16 @@ class WorkloadRun:
         self.p.close()
 
 
-def graph_step_us(w: synth.Workload, dev, rank: int, n: int = 20, reps: int = 5) -> float:
+def graph_step_us(w: synth.Workload, dev, rank: int, n: int = 200) -> dict:
     """An LL workload's step (route, dispatch, combine: no host synchronisation)
-    captured n times in one CUDA graph on a side stream and replayed: the
-    microseconds per step without host launches (how a decode loop runs it)."""
+    replayed from a CUDA graph on a side stream, without host launches (how a
+    decode loop runs it): `us`, a one-step graph replayed n times, each replay
+    between its own events after an L2 flush (when the step is smaller than
+    L2), the mean; `us_l2_warm` (context), a graph of 20 steps replayed back
+    to back, per step."""
     import torch
     s = torch.cuda.Stream(dev)
+    out = {}
     with torch.cuda.stream(s):
         r = WorkloadRun(w, dev, s, rank)
         for _ in range(3):
@@ -469,23 +534,36 @@ def graph_step_us(w: synth.Workload, dev, rank: int, n: int = 20, reps: int = 5)
         torch.cuda.synchronize(dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            for _ in range(n):
-                r.step()
+            r.step()
         g.replay()
         torch.cuda.synchronize(dev)
-        t = []
-        for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            for _ in range(10):
-                g.replay()
-            b.record(s)
-            torch.cuda.synchronize(dev)
-            t.append(a.elapsed_time(b) * 1e3 / (10 * n))
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        eb = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            r.flush_l2()
+            ea[i].record(s)
+            g.replay()
+            eb[i].record(s)
+        torch.cuda.synchronize(dev)
+        out["us"] = statistics.mean(ea[i].elapsed_time(eb[i]) * 1e3 for i in range(n))
         del g
+        g20 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g20, stream=s):
+            for _ in range(20):
+                r.step()
+        g20.replay()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(10):
+            g20.replay()
+        b.record(s)
+        torch.cuda.synchronize(dev)
+        out["us_l2_warm"] = a.elapsed_time(b) * 1e3 / 200
+        del g20
         r.close()
-    return statistics.median(t)
+    return out
 
 
 def secondary_line(w: synth.Workload, r: dict, steps: int) -> dict:
@@ -514,7 +592,10 @@ def secondary_line(w: synth.Workload, r: dict, steps: int) -> dict:
             "route_layout_query_us_by_difference": (step_ms - d - c) * 1e3,
             "event_timing": "route, dispatch and combine each between CUDA events (no launch "
                             "overlap) in one more pass of K steps",
-            "algorithmic_bytes": ab, "back_to_back": r.get("b2b"), "clocks": r["clocks"]}
+            "algorithmic_bytes": ab, "l2": workload_config(w, 1, w.recv_rows())["l2"],
+            **({"step_us_l2_warm": r["warm_pass_ms"] / steps * 1e3}
+               if r.get("warm_pass_ms") is not None else {}),
+            "back_to_back": r.get("b2b"), "clocks": r["clocks"]}
 
 
 def run_gpu(args) -> dict | None:
@@ -636,8 +717,8 @@ def run_gpu(args) -> dict | None:
     del sc_d, x_d, out_d, steps_b, run, p
     torch.cuda.empty_cache()
     link = measure_link(dev) if world == 1 else None   # one process: nothing else on the link
-    graph_us = (graph_step_us(w, dev, rank)
-                if w.mode == synth.MODE_LL and not args.no_b2b and world == 1 else None)
+    graph = (graph_step_us(w, dev, rank)
+             if w.mode == synth.MODE_LL and not args.no_b2b and world == 1 else None)
 
     # --- the other workloads, same process and GPU, one line's `secondary`
     secondary = {}
@@ -654,7 +735,9 @@ def run_gpu(args) -> dict | None:
             torch.cuda.empty_cache()
             secondary[name] = secondary_line(ws, r2, args.steps)
             if ws.mode == synth.MODE_LL and not args.no_b2b:
-                secondary[name]["step_graph_us"] = graph_step_us(ws, dev, rank)
+                gr = graph_step_us(ws, dev, rank)
+                secondary[name]["step_graph_us"] = gr["us"]
+                secondary[name]["step_graph_us_l2_warm"] = gr["us_l2_warm"]
                 torch.cuda.empty_cache()
 
     if world > 1:
@@ -673,8 +756,11 @@ def run_gpu(args) -> dict | None:
         e2e["link_frac_of_both"] = e2e["link_GBps"] / link["both_GBps"]
     line = _line(args, w, world, ms, d_ms, c_ms, clk, w.recv_rows(), ht, e2e, rt, None)
     line["breakdown"]["back_to_back"] = b2b
-    if graph_us is not None:
-        line["breakdown"]["step_graph_us"] = graph_us
+    if graph is not None:
+        line["breakdown"]["step_graph_us"] = graph["us"]
+        line["breakdown"]["step_graph_us_l2_warm"] = graph["us_l2_warm"]
+    if r.get("warm_pass_ms") is not None:
+        line["breakdown"]["step_us_l2_warm"] = r["warm_pass_ms"] / args.steps * 1e3
     if secondary:
         line["secondary"] = secondary
     return line
@@ -716,7 +802,10 @@ def _line(args, w, world, ms, d_ms, c_ms, clk, rows, ht, e2e, rt, nd):
                    "how": "passes of exactly K steps, each bracketed by a barrier and a "
                           "synchronize and timed with CUDA events on the launching stream, "
                           "repeated until >= --min-seconds of GPU time; ms_per_step is the "
-                          "median pass / K (max over ranks)",
+                          "median pass / K (max over ranks)" +
+                          ("; a step smaller than L2: the L2 flushed before every step and "
+                           "each step timed between its own events, a pass being their sum"
+                           if flushes_l2(w) else ""),
                    "sm_kcycles_per_step": (ms / args.steps * clk["sm_mhz"]
                                            if clk.get("sm_mhz") else None)},
         "breakdown": {
