@@ -76,7 +76,10 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
 // thread and an SM holds as many bytes of token rows in flight as with wider
 // rows.  early: x was complete before the layout's producer started, so the
 // first pass is read before waiting for that producer (while the router
-// finishes the layout).
+// finishes the layout).  The token is read with the evict-first policy: it
+// is read once, and the L2 it does not take keeps more of the rows just
+// written for a consumer that reads them back (4096 x 7168, k = 8: step
+// 157.2 -> 156.7 us; 8192 x 4096, k = 2: 65.2 -> 64.1 us).
 template <int U, int NT>
 __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
     RowArgs ra, const uint4* __restrict__ x, int nvec, TokenSplit split, int32_t* __restrict__ row,
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int v = pass + threadIdx.x + u * NT;
-            if (v < ve) buf[u] = __ldg(xt + v);
+            if (v < ve) buf[u] = __ldcs(xt + v);  // read once: evict first
         }
     };
     auto store = [&](int pass) {
