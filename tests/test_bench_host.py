@@ -110,3 +110,20 @@ def test_numa_of_buffer_reads_this_process():
     if "unknown" not in nodes:
         assert sum(nodes.values()) >= 1
     assert bench.gpu_numa_node(None) is None
+
+
+def test_small_steps_flush_the_l2():
+    """Workloads whose step touches less than twice the L2 (the LL ones) are
+    timed step by step after an L2 flush; the large ones stream from HBM."""
+    import bench
+    from combine_layout_gb300 import synth
+    W = synth.WORKLOADS
+    for name in ("tiny_ll", "ll_decode"):
+        assert bench.flushes_l2(W[name]), name
+        assert "flushed" in bench.workload_config(W[name], 1, W[name].recv_rows())["l2"]
+    for name in ("ht_prefill", "ht_prefill_fp8", "mixtral", "skewed"):
+        assert not bench.flushes_l2(W[name]), name
+        assert bench.step_bytes(W[name]) > 2 * bench.L2_BYTES_NOMINAL
+    # the per-step bytes are the three kernels' algorithmic bytes
+    ab = bench.algorithmic_bytes(W["ll_decode"])
+    assert bench.step_bytes(W["ll_decode"]) == ab["route"] + ab["dispatch"] + ab["combine"]
