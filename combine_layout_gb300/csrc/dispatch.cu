@@ -7,7 +7,9 @@
 // one scale per 128 elements.  Here the "send" to logical rank r is a store
 // into rank r's rows of the receive buffer in this GPU's memory.
 //
-// HBM-bound (read 2H bytes per token, write k rows).  One CTA per token: its
+// HBM-bound (read 2H bytes per token, write k rows).  One CTA per token (or
+// per column slice of a token: every token of a small batch, the last few
+// hundred tokens of a large bf16 batch): its
 // threads start reading the token (16-byte vectors, all in flight at once)
 // and warp 0 computes the k pair rows from the layout and stores the row map
 // (bf16: while the token's loads are in flight; FP8: after its own share of
@@ -68,8 +70,8 @@ __device__ __forceinline__ void place_token(const RowArgs& ra, int t, int32_t* r
 // One CTA per work item: a token's row or one of its equal column slices
 // (split: small batches slice every token, so several CTAs share a token's
 // rows; large batches slice only the last few hundred tokens, which shortens
-// the launch's tail; the grid is exactly one CTA per item).  U vectors per thread per
-// pass: the slice's own count where it fits in one pass, so no registers are
+// the launch's tail; the grid is exactly one CTA per item).  U vectors per
+// thread per pass: the slice's own count where it fits in one pass, so no registers are
 // held for vectors a row does not have (fewer registers, more CTAs per SM and
 // more of the token rows in flight).  NT threads: 128, or 64 for rows of at
 // most 512 vectors (H <= 4096), so that a CTA still holds U = 8 vectors per
