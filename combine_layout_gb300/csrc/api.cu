@@ -65,6 +65,7 @@ struct moe_ep_handle {
     int64_t host_total;   // total rows known on the host (-1: not queried)
     int align;            // HT expert blocks padded to a multiple of align rows
     int x_early;          // x is complete before the route (moe_ep_set_x_before_route)
+    int captured;         // the last route was recorded into a CUDA graph (stream capture)
     // send-only operations (staged execution): the send kernels' CTA arrival
     // counter and the signal their last CTA adds 1 to (device workspace), the
     // event recorded after the last send, and the sends not yet completed
@@ -343,6 +344,7 @@ int moe_ep_create_handle(moe_ep_group_t g, int max_topk, moe_ep_handle_t* out)
     h->host_total = -1;
     h->align = 1;
     h->x_early = 0;
+    h->captured = 0;
     g->handles += 1;
     *out = h;
     return MOE_EP_OK;
@@ -373,6 +375,13 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (T > g->S) return MOE_EP_ERR_OVERFLOW;
     if (T > 0 && !topk_idx) return MOE_EP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
+    // a route recorded into a CUDA graph publishes its counts with the
+    // sequence number of the capture on every replay (see the query)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusNone;
+    }
     LayoutArgs la = layout_args(h, T);
     // LL batches of at most kDeferMaxTiles tiles: no serial tail after the
     // router; the dispatch's first CTA finishes the counts and offsets
@@ -422,6 +431,7 @@ int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_tokens,
     if (st != MOE_EP_OK) return st;
     if (la.host_out) h->seq = la.seq;
     h->routed = 1;
+    h->captured = (cap == cudaStreamCaptureStatusActive) ? 1 : 0;
     h->rows_ready = 0;
     h->words_only = la.deferred;
     h->layout_pending = la.deferred;
@@ -453,7 +463,21 @@ int moe_ep_get_num_recv_tokens(moe_ep_handle_t h, int64_t* total, int32_t* per_r
     // the rest of the stream), checking the stream now and then for errors.
     cudaStream_t s = (cudaStream_t)stream;
     const int E = g->E, R = g->R;
-    if (h->T > 0) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusNone;
+    }
+    if (cap == cudaStreamCaptureStatusActive) return MOE_EP_ERR_INVALID;  // a host wait
+    if (h->T > 0 && h->captured) {
+        // every replay of the captured route publishes the same sequence
+        // number, so it cannot tell one replay's counts from the last one's:
+        // wait for the stream (the replays on it) instead
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_EP_ERR_CUDA;
+        const volatile unsigned* seq_word =
+            reinterpret_cast<const volatile unsigned*>(h->host_counts + E + 1 + R + E);
+        if (__atomic_load_n(seq_word, __ATOMIC_ACQUIRE) != h->seq) return MOE_EP_ERR_INVALID;
+    } else if (h->T > 0) {
         volatile unsigned* seq_word = reinterpret_cast<volatile unsigned*>(h->host_counts + E + 1 + R + E);
         const auto t0 = std::chrono::steady_clock::now();
         for (uint64_t it = 1;; ++it) {

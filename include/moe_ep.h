@@ -147,7 +147,13 @@ MOE_EP_API int moe_ep_route(moe_ep_handle_t h, const float* scores, int num_toke
  * itself, so the call waits (host-side) for that layout only, not for work
  * queued after it (a dispatch or combine already launched keeps running); on
  * an error or a stall of more than 10 s it falls back to synchronising the
- * device.  `stream` is only used for that check.  LL: returns the fixed
+ * device.  `stream` is only used for that check.  HT forward recorded into a
+ * CUDA graph (the handle's last moe_ep_route was called during a stream
+ * capture): every replay publishes the counts under the same sequence number,
+ * so the call synchronises `stream` -- pass the stream the graph is replayed
+ * on -- and returns the counts of the last replay that completed on it
+ * (MOE_EP_ERR_INVALID if none has run yet).  Called while `stream` is being
+ * captured (a host wait cannot be recorded): MOE_EP_ERR_INVALID.  LL: returns the fixed
  * capacity without any synchronisation ("低延迟模式": no count exchange):
  * total = E * S, per_rank[r] = L * S, per_expert[e] = S.
  * total, per_rank, per_expert: host pointers (per_rank/per_expert may be NULL). */

@@ -347,3 +347,54 @@ def test_ll_caller_routing_masked_repeated_and_invalid(T):
     assert np.all(bf16_bits(out)[7] == 0)
     assert p.device_errors() == 0
     p.close()
+
+
+def test_ht_forward_replayed_from_a_cuda_graph():
+    """An HT route + dispatch + combine recorded into a CUDA graph and replayed
+    on new inputs (written into the captured buffers): every replay's routing,
+    counts and combined tokens against the oracle.  Each replay publishes its
+    counts under the sequence number of the capture, so the receive-count
+    query after a replay waits for the replay's stream and returns that
+    replay's counts, not the previous one's; during the capture the query is
+    refused (a host wait cannot be recorded)."""
+    ep = _ep()
+    w = synth.WORKLOADS["ht_prefill"].with_tokens(300)
+    p = _pipe(w.mode, w.E, w.R, w.T, w.H, w.k)
+    s = torch.cuda.Stream(DEV)
+    first = synth.make_inputs(w, 700)
+    scores = torch.from_numpy(first["scores"]).to(DEV)
+    x = to_dev_bf16(first["x"], DEV)
+    out = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device=DEV)
+
+    def forward():
+        p.route(scores, w.T, w.G, w.kg, 0, w.weight_mode, stream=s)
+        p.dispatch(x, stream=s)
+        p.combine(p.recv_x, out=out, stream=s)
+
+    with torch.cuda.stream(s):
+        forward()                               # eager, outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        forward()
+        with pytest.raises(ep.MoeEpError) as e:
+            p.num_recv_tokens(stream=s)
+        assert e.value.status == ep.MOE_EP_ERR_INVALID
+    torch.cuda.synchronize()
+    for i in range(3):
+        inp = synth.make_inputs(w, 710 + i)
+        scores.copy_(torch.from_numpy(inp["scores"]))
+        x.copy_(to_dev_bf16(inp["x"], DEV))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        total, per_rank, per_expert = p.num_recv_tokens(stream=s)
+        idx_o, _ = oracle.route(inp["scores"], w.k, w.G, w.kg, weight_mode=w.weight_mode)
+        L_o, st = oracle.layout(idx_o, w.E, w.R, w.mode, w.slots)
+        assert st == oracle.OK
+        assert total == w.T * w.k
+        assert per_rank == L_o["rcnt"].tolist() and per_expert == L_o["cnt"].tolist(), i
+        torch.cuda.synchronize()
+        assert np.array_equal(p.topk_idx[: w.T].cpu().numpy(), idx_o), i
+        assert bf16_ulp_diff(bf16_bits(out), inp["x"]).max() <= 1, i
+    p.close()
